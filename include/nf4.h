@@ -1,0 +1,176 @@
+/*
+ * nf4.h -- C ABI of libnf4: NF4 weight-quantized projections on GB300 (sm_103a).
+ *
+ * The operation (source: "Decode V2 -- resident executor", section 6 "Linear
+ * primitive" and section 3 "CPU oracle"): y = W_hat . x, where W_hat is an
+ * NF4 block-quantized M x K matrix dequantized on the fly,
+ *
+ *     W_hat[m][k] = codebook[code(m, k)] * scales[m][k / 64]     (fp32)
+ *
+ * with the decode step's fused epilogues (residual add for o/down, SwiGLU over
+ * paired gate/up projections, greedy argmax over lm_head rows) and the prefill
+ * chunk (N <= 32 tokens read each weight once; section 0 "Goals" item 1).
+ *
+ * Data layout (all row-major, rows contiguous along K):
+ *   codes  uint8 [M][K/2]   byte j of row m holds k = 2j in bits 0-3 and
+ *                           k = 2j+1 in bits 4-7 ("low nibble = even k")
+ *   scales fp32  [M][K/64]  one absmax scale per 64-weight block along K
+ *   codebook                the 16 NormalFloat levels, ascending, cb[7] = 0,
+ *                           cb[0] = -1, cb[15] = +1 (nf4_codebook)
+ *   bf16 tensors are passed as uint16_t bit patterns.
+ *
+ * Conventions (section 4 "GPU state": arena allocated at load, no cudaMalloc,
+ * .item() or host sync between layers; section 5: the step is captured in a
+ * CUDA graph; "golang.design/x/accel/tensor", Overview: "you own the buffers
+ * you named"):
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The library
+ *     allocates nothing per call, keeps no per-call host state, never
+ *     synchronizes, and launches its kernels asynchronously on `stream`
+ *     (a cudaStream_t; NULL is the legacy default stream).  Calls can be
+ *     recorded into a CUDA graph.
+ *   - Inputs are never written, except that nf4_gemv_residual's `y` may alias
+ *     `residual`.  Any other overlap between an output and an input is
+ *     undefined behaviour.
+ *   - Arguments are validated on the host before any launch; a failed call
+ *     launches nothing and returns a negative nf4_status.  nf4_last_error()
+ *     gives a message for the calling thread's last failure.  Kernels do not
+ *     report errors; invalid device pointers are undefined behaviour.
+ *   - Alignment: codes and x / X must be 16-byte aligned; scales, y, residual,
+ *     logits and Y 4-byte aligned; out 2-byte; index and workspace 8-byte.
+ *   - Sizes: K a positive multiple of 64 and at most NF4_MAX_K; 1 <= M < 2^31.
+ *   - Weights and activations must be finite; NaN/Inf inputs give unspecified
+ *     (but memory-safe) results.
+ */
+#ifndef NF4_H
+#define NF4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest K the kernels accept (elements). */
+#define NF4_MAX_K 65536
+/* Largest token count of the prefill chunk (LIVE_MAX_N in the source page). */
+#define NF4_MAX_CHUNK_N 32
+
+typedef void* nf4_stream; /* a cudaStream_t */
+
+/* One NF4 matrix: device pointers to its codes and scales, and its shape. */
+typedef struct nf4_weight {
+  const uint8_t* codes; /* [M][K/2] */
+  const float* scales;  /* [M][K/64] */
+  int64_t M;
+  int64_t K;
+} nf4_weight;
+
+typedef enum nf4_status {
+  NF4_OK = 0,
+  NF4_EINVAL = -1, /* bad shape: K % 64, K > NF4_MAX_K, M < 1, N outside [1, 32], bad dtype */
+  NF4_EALIGN = -2, /* a pointer is not aligned as stated above */
+  NF4_ENULL = -3,  /* a required pointer is NULL */
+  NF4_ECUDA = -4,  /* a CUDA runtime call or launch failed; see nf4_last_error() */
+  NF4_EARCH = -5   /* the current device is not compute capability 10.3 (sm_103a) */
+} nf4_status;
+
+/* Activation element type. */
+typedef enum nf4_dtype { NF4_F32 = 0, NF4_BF16 = 1 } nf4_dtype;
+
+/*
+ * y[m] = sum_k W_hat[m][k] * x[k]   (N = 1 GEMV, fp32 out)
+ * Source: "Decode V2 -- resident executor", section 6: the gemv backend, FP32
+ * LUT x scale x x; N=1 passes a [K] view.
+ *   W       weight (device codes/scales), shape M x K
+ *   x       [K] activation, fp32 or bf16 (widened exactly to fp32)
+ *   y       [M] fp32 output
+ * Accumulation is fp32; |y - y_exact| <= 2e-3 * sum_k |x_k * W_hat[m][k]|.
+ * The result for a row depends only on that row's codes, scales and x (not on
+ * its position), so identical rows give bit-identical outputs.
+ */
+nf4_status nf4_gemv(const nf4_weight* W, const void* x, nf4_dtype xt, float* y, nf4_stream stream);
+
+/*
+ * y[m] = sum_k W_hat[m][k] * x[k] + residual[m]
+ * Source: same page, section 6: "o/down residual: gemv with add aliased to y".
+ *   residual  [M] fp32; may be the same pointer as y (in-place residual add)
+ */
+nf4_status nf4_gemv_residual(const nf4_weight* W, const void* x, nf4_dtype xt, const float* residual,
+                             float* y, nf4_stream stream);
+
+/*
+ * out[m] = bf16( silu(g_m) * u_m ),  g = Wg . x,  u = Wu . x,  silu(z) = z / (1 + e^-z)
+ * Source: same page, section 6 ("gate+up pairs share x ... writes silu(g)*u")
+ * and section 3 (SiLU after the full gate GEMM, never on a split-K partial);
+ * SiLU evaluated in fp32 ("golang.design/x/accel/tensor", func SiLU).
+ *   Wg, Wu  gate and up weights, identical M and K
+ *   out     [M] bf16 bits, round to nearest even
+ */
+nf4_status nf4_gemv_swiglu(const nf4_weight* Wg, const nf4_weight* Wu, const void* x, nf4_dtype xt,
+                           uint16_t* out, nf4_stream stream);
+
+/*
+ * logits[m] = sum_k W_hat[m][k] * x[k];  *index = min{ m : logits[m] = max_j logits[j] }
+ * Source: same page, section 5 (final lm_head -> next_token = argmax(logits),
+ * the id stays on the device) and "golang.design/x/accel/tensor", func Argmax
+ * ("Ties go to the lowest index").  One launch, no second pass over the logits:
+ * every block folds its rows into a 64-bit (value, index) key with one atomic
+ * max, and the last block to finish writes *index and re-zeroes the workspace.
+ *   logits     [M] fp32 output (the values the argmax is taken over; +0 and
+ *              -0 compare equal)
+ *   index      one int64 on the device
+ *   workspace  nf4_workspace_bytes(M, K, 1) bytes of device memory, zeroed by
+ *              the caller ONCE before its first use; every call leaves it
+ *              zeroed again.  Calls that share a workspace must not overlap in
+ *              time (use one workspace per stream).
+ */
+nf4_status nf4_gemv_argmax(const nf4_weight* W, const void* x, nf4_dtype xt, float* logits,
+                           int64_t* index, void* workspace, nf4_stream stream);
+
+/*
+ * Y[n][m] = sum_k X[n][k] * bf16(W_hat[m][k])   for n < N <= 32, fp32 accumulate
+ * Source: same page, section 0 item 1 and section 5 (prefill walks the prompt
+ * in chunks of LIVE_MAX_N = 32 through the tensor-core GEMM); each weight is
+ * read once per chunk.  The dequantized weight is rounded to bf16 (nearest
+ * even) and multiplied on the tcgen05 tensor cores with fp32 accumulation.
+ *   X          [N][K] bf16 bits, K contiguous
+ *   Y          [N][M] fp32
+ *   workspace  nf4_workspace_bytes(M, K, N) bytes, zeroed once by the caller;
+ *              every call leaves it zeroed again (same sharing rule as above)
+ */
+nf4_status nf4_gemm_chunk(const nf4_weight* W, const uint16_t* X, int N, float* Y, void* workspace,
+                          nf4_stream stream);
+
+/* Workspace bytes that nf4_gemv_argmax (N = 1) or nf4_gemm_chunk (N > 1) need
+ * for an M x K weight; the caller allocates it once (arena). */
+size_t nf4_workspace_bytes(int64_t M, int64_t K, int N);
+
+/*
+ * Quantize fp32 weights W [M][K] to NF4 on the device: per 64-block the scale
+ * is max |w| (an all-zero block gets scale 0 and code 7, the exact-zero level);
+ * each weight takes the level nearest to w / scale, ties to the lower level.
+ * Source: "Decode V2 -- resident executor", section 2 (NF4 linears, 64-weight
+ * groups, encode_nf4 as the one codec).  Not on the decode hot path; provided
+ * so weights can be converted on the device.
+ *   codes [M][K/2] uint8 out, scales [M][K/64] fp32 out
+ */
+nf4_status nf4_quantize(const float* W, int64_t M, int64_t K, uint8_t* codes, float* scales,
+                        nf4_stream stream);
+
+/* Host copy of the 16 fp32 codebook levels the kernels use. Never fails. */
+void nf4_codebook(float out[16]);
+
+/* Message for the calling thread's most recent failed call ("" if none). */
+const char* nf4_last_error(void);
+
+/* Human-readable kernel configuration chosen for an M x K weight at N tokens
+ * (block shape, rows per block, split), or a message if the shape is invalid.
+ * The string is thread-local and valid until the next call on this thread. */
+const char* nf4_describe_config(int64_t M, int64_t K, int N);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NF4_H */

@@ -1,0 +1,339 @@
+/*
+ * nf4_oracle.c -- plain CPU oracle for NF4 weight-quantized projections.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline / reference leg load this library.  The product
+ * library (the CUDA path) never includes, links or calls anything here, and
+ * this file includes nothing from the product.
+ *
+ * Source: "Decode V2 -- resident executor" (deep-fold docs/decode-v2.md),
+ *   section 2 "Synthetic models" (linears are NF4, dims are multiples of the
+ *   64-weight NF4 group), section 3 "CPU oracle" (decode_nf4 then matmul;
+ *   SwiGLU = silu(gate) * up with SiLU applied to the full gate sum; greedy id =
+ *   argmax of the logits), section 6 "Linear primitive" (FP32 LUT x scale x x;
+ *   N=1 takes a [K] view; o/down add a residual into y; prefill chunks of 32).
+ * Argmax tie rule: golang.design/x/accel/tensor, "func Argmax", paragraph
+ *   "Ties go to the lowest index".
+ * bf16 -> f32 widening is exact: same page, "func Cast", "bf16 widens and does
+ *   not narrow".
+ *
+ * Readings where the pages are silent (each one is listed in the design notes):
+ *  - codebook: the 16 NormalFloat levels of the QLoRA construction (Dettmers et
+ *    al. 2023, section 3): quantiles of N(0,1) at evenly spaced probabilities,
+ *    8 on the positive side, 7 on the negative side, plus an exact 0, divided by
+ *    the largest, sorted ascending.  Computed here in float64 with an inverse
+ *    normal CDF found by bisection on Phi(z) = erfc(-z/sqrt 2)/2, then rounded
+ *    once to fp32.
+ *  - encoder: scale = absmax of the 64-block (fp32, exact); an all-zero block
+ *    gets scale 0 and code 7 (the exact-zero level); otherwise each weight takes
+ *    the level nearest to w/scale in exact arithmetic, ties to the lower index.
+ *  - layout: codes[M][K/2], byte j of a row holds k=2j in bits 0-3 and k=2j+1
+ *    in bits 4-7; scales[M][K/64] fp32; rows K-contiguous.
+ *  - dequant: W_hat[m][k] = fp32(cb[code] * scale) (one fp32 rounding).
+ *  - sums: float64, k ascending; epilogues in float64 from the float64 sums,
+ *    rounded once to the output type (round to nearest even).
+ *  - prefill chunk: the weight is dequantized to bf16 (RN of the fp32 W_hat)
+ *    before the product, as the chunk's tensor-core path does; the sum is float64.
+ *
+ * No blocking, fusion or reordering beyond these definitions.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#define NF4O_OK 0
+#define NF4O_EINVAL (-1)
+
+/* x / X element types, same numbering as the public API uses for activations. */
+#define NF4O_F32 0
+#define NF4O_BF16 1
+
+/* ---------------------------------------------------------------- codebook */
+
+/* Phi(z) for the standard normal distribution, through libm's erfc. */
+static double std_normal_cdf(double z) { return 0.5 * erfc(-z / sqrt(2.0)); }
+
+/* Inverse of Phi by bisection: the z with Phi(z) = p, to double resolution. */
+static double std_normal_quantile(double p) {
+  double lo = -40.0, hi = 40.0;
+  for (int it = 0; it < 2000; ++it) {
+    double mid = 0.5 * (lo + hi);
+    if (mid == lo || mid == hi) break;
+    if (std_normal_cdf(mid) < p)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return 0.5 * (lo + hi);
+}
+
+/* The 16 NF4 levels, ascending, fp32.  cb[0] = -1, cb[7] = 0, cb[15] = +1. */
+int nf4o_codebook(float cb[16]) {
+  const double delta = 0.5 * (1.0 / 32.0 + 1.0 / 30.0);
+  double v[16];
+  int n = 0;
+  /* 8 levels on the positive side: probabilities from 1-delta down towards 1/2 */
+  for (int j = 0; j < 8; ++j) v[n++] = std_normal_quantile(1.0 - delta - j * (0.5 - delta) / 8.0);
+  /* 7 levels on the negative side: probabilities from delta up towards 1/2 */
+  for (int j = 0; j < 7; ++j) v[n++] = std_normal_quantile(delta + j * (0.5 - delta) / 7.0);
+  v[n++] = 0.0;
+  const double top = std_normal_quantile(1.0 - delta);
+  for (int i = 0; i < 16; ++i) v[i] /= top;
+  /* insertion sort, ascending */
+  for (int i = 1; i < 16; ++i) {
+    double t = v[i];
+    int j = i - 1;
+    while (j >= 0 && v[j] > t) {
+      v[j + 1] = v[j];
+      --j;
+    }
+    v[j + 1] = t;
+  }
+  for (int i = 0; i < 16; ++i) cb[i] = (float)v[i];
+  return NF4O_OK;
+}
+
+/* ------------------------------------------------------------- bit helpers */
+
+static float bf16_bits_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* Round a double to the nearest bf16 (ties to even); returns the bits. */
+static uint16_t f64_to_bf16_bits(double v) {
+  if (isnan(v)) return 0x7FC0;
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e); /* a = m * 2^e, m in [0.5, 1) */
+  /* bf16 keeps 8 significant bits; its smallest normal is 2^-126 and its
+   * subnormals step by 2^-133. */
+  int q = e - 8;
+  if (q < -133) q = -133;
+  double r = rint(ldexp(a, -q)); /* default rounding mode: to nearest even */
+  double rv = ldexp(r, q);
+  /* re-encode rv: exactly representable in bf16 unless it rounded up to 2^128 */
+  if (rv > 3.3895313892515355e38 /* largest finite bf16, (2 - 2^-7) * 2^127 */) return sign | 0x7F80;
+  float f = (float)rv; /* exact: rv has <= 8 significant bits within fp32 range */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(sign | ((u >> 16) & 0x7FFF));
+}
+
+/* Round an fp32 to the nearest bf16 (ties to even); returns the value as fp32. */
+static float f32_round_bf16(float f) { return bf16_bits_to_f32(f64_to_bf16_bits((double)f)); }
+
+static double load_x(const void* x, int xt, int64_t k) {
+  if (xt == NF4O_BF16) return (double)bf16_bits_to_f32(((const uint16_t*)x)[k]);
+  return (double)((const float*)x)[k];
+}
+
+static int code_at(const uint8_t* codes, int64_t K, int64_t m, int64_t k) {
+  uint8_t byte = codes[m * (K / 2) + k / 2];
+  return (k & 1) ? (byte >> 4) : (byte & 0x0F);
+}
+
+static float what_at(const float cb[16], const uint8_t* codes, const float* scales, int64_t K, int64_t m,
+                     int64_t k) {
+  float c = cb[code_at(codes, K, m, k)];
+  float s = scales[m * (K / 64) + k / 64];
+  return c * s; /* one fp32 rounding */
+}
+
+static int shape_ok(int64_t M, int64_t K) { return M >= 1 && K >= 64 && K % 64 == 0; }
+
+/* ----------------------------------------------------------------- encoder */
+
+/*
+ * Nearest level to w/s with ties to the lower index, decided exactly.
+ * The tie point between levels i and i+1 is mid_i = (cb[i] + cb[i+1]) / 2.
+ * w/s > mid_i  <=>  w > mid_i * s  for s > 0, and both mid_i and mid_i * s are
+ * exact in float64 (cb values carry 24 significant bits, their sums at most 26,
+ * the product with a 24-bit scale at most 50), so the comparison below is the
+ * exact-arithmetic one.  The code is the number of tie points strictly below.
+ */
+static int nearest_code(const float cb[16], float w, float s) {
+  int code = 0;
+  for (int i = 0; i < 15; ++i) {
+    double mid = ((double)cb[i] + (double)cb[i + 1]) / 2.0;
+    if ((double)w > mid * (double)s) ++code;
+  }
+  return code;
+}
+
+int nf4o_quantize(const float* W, int64_t M, int64_t K, uint8_t* codes, float* scales) {
+  if (!shape_ok(M, K) || !W || !codes || !scales) return NF4O_EINVAL;
+  float cb[16];
+  nf4o_codebook(cb);
+  const int64_t nb = K / 64;
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* w = W + m * K + b * 64;
+      float s = 0.0f;
+      for (int i = 0; i < 64; ++i) {
+        if (!isfinite(w[i])) return NF4O_EINVAL;
+        float a = fabsf(w[i]);
+        if (a > s) s = a;
+      }
+      scales[m * nb + b] = s;
+      uint8_t* out = codes + m * (K / 2) + b * 32;
+      for (int j = 0; j < 32; ++j) {
+        int lo = (s == 0.0f) ? 7 : nearest_code(cb, w[2 * j], s);
+        int hi = (s == 0.0f) ? 7 : nearest_code(cb, w[2 * j + 1], s);
+        out[j] = (uint8_t)(lo | (hi << 4));
+      }
+    }
+  }
+  return NF4O_OK;
+}
+
+/* ------------------------------------------------------------------ decode */
+
+int nf4o_dequant(const uint8_t* codes, const float* scales, int64_t M, int64_t K, float* W_hat) {
+  if (!shape_ok(M, K) || !codes || !scales || !W_hat) return NF4O_EINVAL;
+  float cb[16];
+  nf4o_codebook(cb);
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t k = 0; k < K; ++k) W_hat[m * K + k] = what_at(cb, codes, scales, K, m, k);
+  return NF4O_OK;
+}
+
+/* --------------------------------------------------------------- N=1 GEMV */
+
+/*
+ * y[i] = sum_k W_hat[m][k] * x[k] in float64, k ascending, for m = rows[i]
+ * (all rows in order when rows is NULL).  S[i] = sum_k |W_hat[m][k] * x[k]|,
+ * the per-row magnitude the tolerance is stated against.  Either output may be
+ * NULL.
+ */
+int nf4o_gemv(const uint8_t* codes, const float* scales, int64_t M, int64_t K, const void* x, int xt,
+              const int64_t* rows, int64_t nrows, double* y, double* S) {
+  if (!shape_ok(M, K) || !codes || !scales || !x) return NF4O_EINVAL;
+  if (xt != NF4O_F32 && xt != NF4O_BF16) return NF4O_EINVAL;
+  if (!rows) nrows = M;
+  float cb[16];
+  nf4o_codebook(cb);
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t m = rows ? rows[i] : i;
+    if (m < 0 || m >= M) return NF4O_EINVAL;
+    double acc = 0.0, mag = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      double t = (double)what_at(cb, codes, scales, K, m, k) * load_x(x, xt, k);
+      acc += t;
+      mag += fabs(t);
+    }
+    if (y) y[i] = acc;
+    if (S) S[i] = mag;
+  }
+  return NF4O_OK;
+}
+
+/* y = W x + r, float64 sum plus the residual, rounded once to fp32. */
+int nf4o_gemv_residual(const uint8_t* codes, const float* scales, int64_t M, int64_t K, const void* x,
+                       int xt, const float* r, const int64_t* rows, int64_t nrows, double* y_f64,
+                       float* y_f32) {
+  if (!r) return NF4O_EINVAL;
+  if (!rows) nrows = M;
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t m = rows ? rows[i] : i;
+    double acc;
+    int st = nf4o_gemv(codes, scales, M, K, x, xt, &m, 1, &acc, NULL);
+    if (st) return st;
+    double v = acc + (double)r[m];
+    if (y_f64) y_f64[i] = v;
+    if (y_f32) y_f32[i] = (float)v;
+  }
+  return NF4O_OK;
+}
+
+/* silu(z) = z / (1 + e^-z), float64 */
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/*
+ * out[i] = silu(g_m) * u_m with g = Wg x and u = Wu x (float64 sums over the
+ * full K), rounded once to bf16.  out_f64 gets the unrounded value, out_bf16
+ * the rounded bits, g/u the float64 sums.  Any output may be NULL.
+ */
+int nf4o_gemv_swiglu(const uint8_t* g_codes, const float* g_scales, const uint8_t* u_codes,
+                     const float* u_scales, int64_t M, int64_t K, const void* x, int xt,
+                     const int64_t* rows, int64_t nrows, double* out_f64, uint16_t* out_bf16,
+                     double* g, double* u) {
+  if (!rows) nrows = M;
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t m = rows ? rows[i] : i;
+    double gs, us;
+    int st = nf4o_gemv(g_codes, g_scales, M, K, x, xt, &m, 1, &gs, NULL);
+    if (st) return st;
+    st = nf4o_gemv(u_codes, u_scales, M, K, x, xt, &m, 1, &us, NULL);
+    if (st) return st;
+    double v = silu(gs) * us;
+    if (out_f64) out_f64[i] = v;
+    if (out_bf16) out_bf16[i] = f64_to_bf16_bits(v);
+    if (g) g[i] = gs;
+    if (u) u[i] = us;
+  }
+  return NF4O_OK;
+}
+
+/*
+ * Greedy argmax over all M rows: logits_f64 (float64 sums, may be NULL),
+ * logits_f32 (each rounded once to fp32, may be NULL) and the index of the
+ * largest float64 logit, ties to the lowest index.
+ */
+int nf4o_gemv_argmax(const uint8_t* codes, const float* scales, int64_t M, int64_t K, const void* x,
+                     int xt, double* logits_f64, float* logits_f32, int64_t* index) {
+  if (!index) return NF4O_EINVAL;
+  int64_t best = -1;
+  double best_v = 0.0;
+  for (int64_t m = 0; m < M; ++m) {
+    double v;
+    int st = nf4o_gemv(codes, scales, M, K, x, xt, &m, 1, &v, NULL);
+    if (st) return st;
+    if (logits_f64) logits_f64[m] = v;
+    if (logits_f32) logits_f32[m] = (float)v;
+    if (best < 0 || v > best_v) { /* strict: an equal later logit never wins */
+      best = m;
+      best_v = v;
+    }
+  }
+  *index = best;
+  return NF4O_OK;
+}
+
+/*
+ * Prefill chunk: Y[n][m] = sum_k bf16(W_hat[m][k]) * X[n][k] in float64,
+ * k ascending, for n < N and m = rows[i] (all rows when rows is NULL).
+ * X is bf16 bits, [N][K] row-major.  Y is [N][nrows] (row-major over n).
+ * S (may be NULL) gets sum_k |bf16(W_hat) * X| with the same layout.
+ */
+int nf4o_gemm_chunk(const uint8_t* codes, const float* scales, int64_t M, int64_t K, const uint16_t* X,
+                    int64_t N, const int64_t* rows, int64_t nrows, double* Y, double* S) {
+  if (!shape_ok(M, K) || !codes || !scales || !X || N < 1) return NF4O_EINVAL;
+  if (!rows) nrows = M;
+  float cb[16];
+  nf4o_codebook(cb);
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t i = 0; i < nrows; ++i) {
+      int64_t m = rows ? rows[i] : i;
+      if (m < 0 || m >= M) return NF4O_EINVAL;
+      double acc = 0.0, mag = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        double w = (double)f32_round_bf16(what_at(cb, codes, scales, K, m, k));
+        double t = w * (double)bf16_bits_to_f32(X[n * K + k]);
+        acc += t;
+        mag += fabs(t);
+      }
+      if (Y) Y[n * nrows + i] = acc;
+      if (S) S[n * nrows + i] = mag;
+    }
+  }
+  return NF4O_OK;
+}
+
+/* Rounding helpers exposed for the tests: double -> bf16 bits (RN-even). */
+uint16_t nf4o_round_bf16(double v) { return f64_to_bf16_bits(v); }

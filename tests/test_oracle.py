@@ -1,0 +1,454 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+Codebook: the closed form of the QLoRA NormalFloat construction evaluated with
+scipy's inverse normal CDF (a library routine) and the table's invariants.
+Encoder: exact rational brute force, round trip, error bound, zero block.
+GEMV: hand-computed worked examples (tests/golden/worked_examples.txt), exact
+sums via math.fsum, numpy float64 matmul, power-of-two linearity, the zero level.
+Epilogues: residual / SwiGLU / argmax reduce to the GEMV plus their definitions;
+argmax ties go to the lowest index ("golang.design/x/accel/tensor", func Argmax).
+Chunk: equals the GEMV exactly when every W_hat is representable in bf16, and
+otherwise stays within the bf16 rounding bound of the weights.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from nf4_weight_quantized_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_examples.txt")
+
+
+# ------------------------------------------------------------------ codebook
+
+def test_codebook_invariants(cb):
+    assert cb.dtype == np.float32 and cb.shape == (16,)
+    assert np.all(np.diff(cb.astype(np.float64)) > 0)
+    assert cb[0] == -1.0 and cb[7] == 0.0 and cb[15] == 1.0
+    assert np.sum(cb > 0) == 8 and np.sum(cb < 0) == 7  # asymmetric: 8 positive, 7 negative
+
+
+def test_codebook_closed_form_matches_scipy(cb):
+    ndtri = pytest.importorskip("scipy.special").ndtri
+    d = 0.5 * (1 / 32 + 1 / 30)
+    pos = ndtri(1 - d - np.arange(8) * (0.5 - d) / 8)
+    neg = ndtri(d + np.arange(7) * (0.5 - d) / 7)
+    ref = (np.sort(np.concatenate([pos, neg, [0.0]])) / ndtri(1 - d)).astype(np.float32)
+    assert np.array_equal(ref.view(np.uint32), cb.view(np.uint32))
+
+
+def test_codebook_values_to_1e6(cb):
+    # the 16 levels, 7 decimals (float64 evaluation of the construction)
+    printed = [-1.0, -0.6961928, -0.5250729, -0.3949175, -0.2844413, -0.1847734, -0.0910500, 0.0,
+               0.0795803, 0.1609302, 0.2461123, 0.3379152, 0.4407097, 0.5626170, 0.7229568, 1.0]
+    assert np.max(np.abs(cb.astype(np.float64) - np.array(printed))) < 1e-6
+
+
+# ------------------------------------------------------------------- encoder
+
+def _exact_nearest(cb, w, s):
+    """Nearest level to w/s in exact rationals, ties to the lower index."""
+    if s == 0:
+        return 7
+    v = Fraction(float(w)) / Fraction(float(s))
+    best, best_d = None, None
+    for i, c in enumerate(cb):
+        dd = abs(v - Fraction(float(c)))
+        if best is None or dd < best_d:
+            best, best_d = i, dd
+    return best
+
+
+def _unpack(codes, K):
+    lo = codes & 0x0F
+    hi = codes >> 4
+    out = np.empty((codes.shape[0], K), np.uint8)
+    out[:, 0::2] = lo
+    out[:, 1::2] = hi
+    return out
+
+
+def _pack(c):
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def test_encoder_exact_bruteforce(oracle_mod, cb):
+    g = np.random.Generator(np.random.PCG64(11))
+    W = (g.standard_normal((3, 128)) * 0.02).astype(np.float32)
+    # plant exact ties: values at the midpoint of two levels times the block absmax
+    s = np.float32(np.max(np.abs(W[0, :64])))
+    for i in range(15):
+        mid = (Fraction(float(cb[i])) + Fraction(float(cb[i + 1]))) / 2 * Fraction(float(s))
+        f = np.float32(float(mid))
+        if Fraction(float(f)) == mid and abs(f) < s:
+            W[0, 2 + i] = f
+    codes, scales = oracle_mod.quantize(W)
+    cu = _unpack(codes, 128)
+    for m in range(3):
+        for b in range(2):
+            blk = W[m, 64 * b:64 * b + 64]
+            s = np.float32(np.max(np.abs(blk)))
+            assert scales[m, b] == s
+            for j in range(64):
+                assert cu[m, 64 * b + j] == _exact_nearest(cb, blk[j], s), (m, b, j)
+
+
+def test_encoder_ties_go_low(oracle_mod, cb):
+    # a block whose absmax is 1 and which holds every exact midpoint of the table
+    # that fp32 can represent: each must map to the lower of its two levels
+    W = np.zeros((1, 64), np.float32)
+    W[0, 0] = 1.0
+    planted = []
+    for i in range(15):
+        mid = (Fraction(float(cb[i])) + Fraction(float(cb[i + 1]))) / 2
+        f = np.float32(float(mid))
+        if Fraction(float(f)) == mid:
+            W[0, 1 + i] = f
+            planted.append((1 + i, i))
+    assert planted, "no representable midpoint"
+    codes, _ = oracle_mod.quantize(W)
+    cu = _unpack(codes, 64)
+    for k, lower in planted:
+        assert cu[0, k] == lower
+
+
+def test_midpoint_products_are_exact(cb):
+    # the encoder compares w against mid_i * s in float64; check that both the
+    # midpoints and their products with fp32 scales carry at most 53 bits
+    g = np.random.Generator(np.random.PCG64(5))
+    scales = np.abs(g.standard_normal(200)).astype(np.float32)
+    for i in range(15):
+        mid = (Fraction(float(cb[i])) + Fraction(float(cb[i + 1]))) / 2
+        assert Fraction((float(cb[i]) + float(cb[i + 1])) / 2) == mid
+        for s in scales:
+            assert Fraction(float(mid) * float(s)) == mid * Fraction(float(s))
+
+
+def test_zero_block(oracle_mod):
+    W = np.zeros((2, 128), np.float32)
+    W[0, 64:] = -0.0
+    W[1, :64] = np.linspace(-1, 1, 64, dtype=np.float32)
+    codes, scales = oracle_mod.quantize(W)
+    assert np.all(codes[0] == 0x77) and np.all(scales[0] == 0.0)
+    assert np.all(codes[1, 32:] == 0x77) and scales[1, 1] == 0.0
+    assert scales[1, 0] == 1.0
+
+
+def test_roundtrip(oracle_mod, cb):
+    g = np.random.Generator(np.random.PCG64(3))
+    M, K = 8, 256
+    c = g.integers(0, 16, size=(M, K)).astype(np.uint8)
+    c[:, ::64] = g.choice([0, 15], size=(M, K // 64))  # every block holds a +-1 level
+    s = (np.abs(g.standard_normal((M, K // 64))) * 0.05 + 1e-3).astype(np.float32)
+    codes = _pack(c)
+    W_hat = oracle_mod.dequant(codes, s)
+    codes2, s2 = oracle_mod.quantize(W_hat)
+    assert np.array_equal(codes2, codes)
+    assert np.array_equal(s2, s)
+
+
+def test_dequant_definition(oracle_mod, cb):
+    g = np.random.Generator(np.random.PCG64(4))
+    M, K = 4, 128
+    c = g.integers(0, 16, size=(M, K)).astype(np.uint8)
+    s = g.standard_normal((M, K // 64)).astype(np.float32)
+    W_hat = oracle_mod.dequant(_pack(c), s)
+    ref = (cb[c] * np.repeat(s, 64, axis=1)).astype(np.float32)  # fp32 product
+    assert np.array_equal(W_hat.view(np.uint32), ref.view(np.uint32))
+
+
+def test_quantization_error_bound(oracle_mod, cb):
+    W = synth.weights(7, 0, 16, 512)
+    codes, scales = oracle_mod.quantize(W)
+    W_hat = oracle_mod.dequant(codes, scales).astype(np.float64)
+    half_gap = np.max(np.diff(cb.astype(np.float64))) / 2  # 0.1519...
+    assert abs(half_gap - 0.15190) < 1e-4
+    s = np.repeat(scales.astype(np.float64), 64, axis=1)
+    assert np.all(np.abs(W.astype(np.float64) - W_hat) <= half_gap * s * (1 + 1e-6))
+
+
+# ---------------------------------------------------------------------- GEMV
+
+def _parse_golden():
+    cases = []
+    cur = None
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, _, rest = line.partition(" ")
+            if head == "case":
+                name, kk = rest.split()
+                cur = {"name": name, "K": int(kk.split("=")[1]), "rows": [], "x": None, "y": None}
+                cases.append(cur)
+            elif head == "row":
+                blocks, scales = rest.split("|")
+                cur["rows"].append((blocks.split(), [float(v) for v in scales.split()]))
+            elif head == "x":
+                cur["x"] = rest
+            elif head == "y":
+                cur["y"] = [float(v) for v in rest.split()]
+    return cases
+
+
+def _build_case(case):
+    K = case["K"]
+    M = len(case["rows"])
+    c = np.zeros((M, K), np.uint8)
+    s = np.zeros((M, K // 64), np.float32)
+    for m, (blocks, scales) in enumerate(case["rows"]):
+        for b, tok in enumerate(blocks):
+            if tok.startswith("alt"):
+                a, bb = (int(v) for v in tok[3:].split(","))
+                c[m, 64 * b:64 * b + 64:2] = a
+                c[m, 64 * b + 1:64 * b + 64:2] = bb
+            else:
+                c[m, 64 * b:64 * b + 64] = int(tok[1:])
+        s[m] = scales
+    rule = case["x"].split()
+    k = np.arange(K)
+    if rule[0] == "ones":
+        x = np.ones(K)
+    elif rule[0] == "k":
+        x = k.astype(np.float64)
+    elif rule[0] == "steps":
+        vals = [float(v) for v in rule[1].split(",")]
+        x = np.array([vals[i // 64] for i in k])
+    elif rule[0] == "onehot":
+        x = np.zeros(K)
+        x[int(rule[1])] = 1.0
+    else:
+        raise ValueError(rule)
+    return _pack(c), s, x.astype(np.float32)
+
+
+@pytest.mark.parametrize("case", _parse_golden(), ids=lambda c: c["name"])
+def test_worked_examples(oracle_mod, case):
+    codes, scales, x = _build_case(case)
+    y, _ = oracle_mod.gemv(codes, scales, x)
+    assert list(y) == case["y"]
+    # same activation as bf16 (all values here are exact in bf16)
+    xb = synth.f32_bits_to_bf16(x)
+    assert np.array_equal(synth.bf16_to_f32(xb), x)
+    yb, _ = oracle_mod.gemv(codes, scales, xb)
+    assert list(yb) == case["y"]
+
+
+def test_sum_of_levels(oracle_mod, cb):
+    # codes 0..15 repeated four times, scale 1, x = 1: y = 4 * sum(cb)
+    c = np.tile(np.arange(16, dtype=np.uint8), 4)[None, :]
+    y, S = oracle_mod.gemv(_pack(c), np.ones((1, 1), np.float32), np.ones(64, np.float32))
+    assert y[0] == math.fsum(4 * [float(v) for v in cb])
+    assert S[0] == math.fsum(4 * [abs(float(v)) for v in cb])
+
+
+def test_gemv_exact_sum(oracle_mod):
+    W = synth.weights(9, 0, 6, 1024)
+    codes, scales = oracle_mod.quantize(W)
+    x = synth.normal_bf16(9, 1, 1024)
+    y, S = oracle_mod.gemv(codes, scales, x)
+    W_hat = oracle_mod.dequant(codes, scales).astype(np.float64)
+    xf = synth.bf16_to_f32(x).astype(np.float64)
+    for m in range(6):
+        terms = W_hat[m] * xf  # exact: fp32 x bf16 products fit in float64
+        assert abs(y[m] - math.fsum(terms)) <= 1e-13 * S[m]
+        assert abs(S[m] - math.fsum(np.abs(terms))) <= 1e-13 * S[m]
+
+
+def test_gemv_vs_numpy_matmul(oracle_mod):
+    W = synth.weights(10, 0, 256, 512)
+    codes, scales = oracle_mod.quantize(W)
+    x = synth.normal_f32(10, 1, 512)
+    y, S = oracle_mod.gemv(codes, scales, x)
+    ref = oracle_mod.dequant(codes, scales).astype(np.float64) @ x.astype(np.float64)
+    assert np.all(np.abs(y - ref) <= 1e-12 * S)
+
+
+def test_gemv_row_subset(oracle_mod):
+    W = synth.weights(12, 0, 64, 256)
+    codes, scales = oracle_mod.quantize(W)
+    x = synth.normal_f32(12, 1, 256)
+    y_all, S_all = oracle_mod.gemv(codes, scales, x)
+    rows = np.array([63, 0, 17, 17, 5])
+    y, S = oracle_mod.gemv(codes, scales, x, rows=rows)
+    assert np.array_equal(y, y_all[rows]) and np.array_equal(S, S_all[rows])
+
+
+def test_gemv_linearity_power_of_two(oracle_mod):
+    W = synth.weights(13, 0, 32, 256)
+    codes, scales = oracle_mod.quantize(W)
+    x = synth.normal_f32(13, 1, 256)
+    y, _ = oracle_mod.gemv(codes, scales, x)
+    for a in (2.0, 0.25, -8.0):
+        ya, _ = oracle_mod.gemv(codes, scales, (x * a).astype(np.float32))
+        assert np.array_equal(ya, y * a)
+
+
+def test_zero_level_rows(oracle_mod):
+    g = np.random.Generator(np.random.PCG64(14))
+    M, K = 4, 192
+    codes = np.full((M, K // 2), 0x77, np.uint8)
+    scales = (g.standard_normal((M, K // 64)) * 100).astype(np.float32)
+    x = g.standard_normal(K).astype(np.float32)
+    y, S = oracle_mod.gemv(codes, scales, x)
+    assert np.all(y == 0.0) and np.all(S == 0.0)
+    r = g.standard_normal(M).astype(np.float32)
+    y64, y32 = oracle_mod.gemv_residual(codes, scales, x, r)
+    assert np.array_equal(y32, r)
+
+
+# ----------------------------------------------------------------- epilogues
+
+def test_residual(oracle_mod):
+    W = synth.weights(15, 0, 64, 256)
+    codes, scales = oracle_mod.quantize(W)
+    x = synth.normal_bf16(15, 1, 256)
+    r = synth.normal_f32(15, 2, 64)
+    y, _ = oracle_mod.gemv(codes, scales, x)
+    y64, y32 = oracle_mod.gemv_residual(codes, scales, x, r)
+    assert np.array_equal(y64, y + r.astype(np.float64))
+    assert np.array_equal(y32, (y + r.astype(np.float64)).astype(np.float32))
+
+
+def _exact_bf16_round(v: float) -> int:
+    """bf16 bits of a finite nonzero double by exact rational rounding (ties to even)."""
+    if v == 0:
+        return 0x8000 if math.copysign(1, v) < 0 else 0
+    sign = 0x8000 if v < 0 else 0
+    a = Fraction(abs(v))
+    e = math.floor(math.log2(abs(v)))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    q = max(e - 7, -133)
+    scaled = a / Fraction(2) ** q
+    r = math.floor(scaled)
+    rem = scaled - r
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and r % 2 == 1):
+        r += 1
+    val = float(Fraction(r) * Fraction(2) ** q)
+    return sign | int(np.array([val], np.float32).view(np.uint32)[0] >> 16)
+
+
+def test_round_bf16(oracle_mod):
+    g = np.random.Generator(np.random.PCG64(16))
+    vals = list(g.standard_normal(300) * 10.0 ** g.integers(-30, 30, 300))
+    # exact ties between two bf16 neighbours (odd and even last bits) and extremes
+    vals += [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 1.5e-40, 2.0 ** -133 * 1.5]
+    for v in vals:
+        assert oracle_mod.round_bf16(v) == _exact_bf16_round(v), v
+    assert oracle_mod.round_bf16(3.4e38) == 0x7F80  # rounds past the largest bf16
+
+
+def test_swiglu(oracle_mod):
+    M, K = 48, 256
+    Wg = synth.weights(17, 0, M, K)
+    Wu = synth.weights(17, 1, M, K)
+    Wg[3] = 0.0  # a zero gate row: silu(0) = 0
+    gc, gs = oracle_mod.quantize(Wg)
+    uc, us = oracle_mod.quantize(Wu)
+    x = synth.normal_bf16(17, 2, K)
+    out64, outbf, g, u = oracle_mod.gemv_swiglu(gc, gs, uc, us, x)
+    yg, _ = oracle_mod.gemv(gc, gs, x)
+    yu, _ = oracle_mod.gemv(uc, us, x)
+    assert np.array_equal(g, yg) and np.array_equal(u, yu)
+    assert out64[3] == 0.0 and outbf[3] in (0, 0x8000)
+    # silu(z) = z * sigmoid(z): compare with an independent logistic form
+    ref = g * (0.5 * (1.0 + np.tanh(0.5 * g))) * u
+    assert np.all(np.abs(out64 - ref) <= 1e-13 * (np.abs(ref) + 1e-30))
+    for i in range(M):
+        assert outbf[i] == _exact_bf16_round(out64[i]) or out64[i] == 0.0
+
+
+def test_swiglu_limits(oracle_mod):
+    # large positive gate: silu(g) -> g; large negative gate: silu(g) -> 0
+    K = 64
+    gc = np.full((2, 32), 0xFF, np.uint8)  # all +1
+    gs = np.array([[1.0], [-1.0]], np.float32)  # row 0: +64, row 1: -64 (x = 1)
+    uc = np.full((2, 32), 0xFF, np.uint8)
+    us = np.array([[0.5], [0.5]], np.float32)  # u = 32
+    x = np.ones(K, np.float32)
+    out64, _, g, u = oracle_mod.gemv_swiglu(gc, gs, uc, us, x)
+    assert g[0] == 64 and g[1] == -64 and u[0] == 32
+    assert abs(out64[0] - 64 * 32) < 1e-9
+    assert abs(out64[1]) < 1e-20
+
+
+def test_argmax_bruteforce_and_ties(oracle_mod):
+    M, K = 300, 256
+    W = synth.weights(18, 0, M, K)
+    codes, scales = oracle_mod.quantize(W)
+    x = synth.normal_bf16(18, 1, K)
+    l64, l32, idx = oracle_mod.gemv_argmax(codes, scales, x)
+    y, _ = oracle_mod.gemv(codes, scales, x)
+    assert np.array_equal(l64, y)
+    assert np.array_equal(l32, y.astype(np.float32))
+    assert idx == int(np.argmax(y)) and y[idx] == y.max()
+    # duplicate the winning row before and after it: the lowest copy wins
+    best = idx
+    lo, hi = best // 2, min(M - 1, best + 7)
+    codes2, scales2 = codes.copy(), scales.copy()
+    for r in (lo, hi):
+        codes2[r], scales2[r] = codes[best], scales[best]
+    _, _, idx2 = oracle_mod.gemv_argmax(codes2, scales2, x)
+    assert idx2 == min(lo, best)
+
+
+def test_argmax_all_equal():
+    import oracle
+
+    codes = np.full((10, 32), 0x77, np.uint8)
+    scales = np.ones((10, 1), np.float32)
+    _, _, idx = oracle.gemv_argmax(codes, scales, np.ones(64, np.float32))
+    assert idx == 0
+
+
+# --------------------------------------------------------------------- chunk
+
+def test_chunk_equals_gemv_when_weights_are_bf16_exact(oracle_mod):
+    g = np.random.Generator(np.random.PCG64(19))
+    M, K, N = 24, 256, 5
+    c = g.choice([0, 7, 15], size=(M, K)).astype(np.uint8)  # levels -1, 0, +1
+    s = (2.0 ** g.integers(-8, 3, size=(M, K // 64))).astype(np.float32)
+    codes = _pack(c)
+    X = synth.normal_bf16(19, 1, N * K).reshape(N, K)
+    Y, S = oracle_mod.gemm_chunk(codes, s, X)
+    for n in range(N):
+        y, Sg = oracle_mod.gemv(codes, s, X[n])
+        assert np.array_equal(Y[n], y) and np.array_equal(S[n], Sg)
+
+
+def test_chunk_bf16_weight_bound(oracle_mod):
+    W = synth.weights(20, 0, 40, 512)
+    codes, scales = oracle_mod.quantize(W)
+    X = synth.normal_bf16(20, 1, 3 * 512).reshape(3, 512)
+    Y, S = oracle_mod.gemm_chunk(codes, scales, X)
+    for n in range(3):
+        y, Sg = oracle_mod.gemv(codes, scales, X[n])
+        # each weight moves by at most 2^-9 relative when rounded to bf16
+        assert np.all(np.abs(Y[n] - y) <= 2.0 ** -9 * Sg * (1 + 1e-9))
+        assert np.any(Y[n] != y)  # the rounding is really applied
+    rows = np.array([39, 2])
+    Yr, _ = oracle_mod.gemm_chunk(codes, scales, X, rows=rows)
+    assert np.array_equal(Yr, Y[:, rows])
+
+
+def test_chunk_explicit_bf16_products(oracle_mod, cb):
+    # small case spelled out: bf16(W_hat) via numpy rounding of the fp32 W_hat
+    W = synth.weights(21, 0, 3, 64)
+    codes, scales = oracle_mod.quantize(W)
+    W_hat = oracle_mod.dequant(codes, scales)
+    Wb = synth.bf16_to_f32(synth.f32_bits_to_bf16(W_hat)).astype(np.float64)
+    X = synth.normal_bf16(21, 1, 2 * 64).reshape(2, 64)
+    Y, _ = oracle_mod.gemm_chunk(codes, scales, X)
+    Xf = synth.bf16_to_f32(X).astype(np.float64)
+    for n in range(2):
+        for m in range(3):
+            assert abs(Y[n, m] - math.fsum(Wb[m] * Xf[n])) <= 1e-14 * np.sum(np.abs(Wb[m] * Xf[n]))
