@@ -1,0 +1,281 @@
+// abi.cu -- the extern "C" boundary of libnf4: validation, device checks,
+// configuration choice and asynchronous launches.  See include/nf4.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "nf4.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local std::string g_describe;
+
+nf4_status fail(nf4_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+// ---------------------------------------------------------------- codebook
+//
+// The 16 NormalFloat levels (QLoRA construction, Dettmers et al. 2023, sec. 3):
+// N(0,1) quantiles at 8 evenly spaced probabilities from 1-d towards 1/2 and
+// 7 from d towards 1/2, d = (1/32 + 1/30) / 2, plus an exact 0, divided by the
+// largest and sorted.  The inverse normal CDF is found here by Newton's method
+// on Phi(z) = erfc(-z / sqrt 2) / 2 started at 0 (Phi is concave above 0 and
+// convex below, so the iterates approach the root from one side), in float64,
+// and each level is rounded once to fp32.
+
+double normal_cdf(double z) { return 0.5 * std::erfc(-z / std::sqrt(2.0)); }
+double normal_pdf(double z) { return std::exp(-0.5 * z * z) / std::sqrt(2.0 * 3.14159265358979323846); }
+
+double normal_quantile(double p) {
+  double z = 0.0;
+  for (int it = 0; it < 100; ++it) {
+    const double dz = (normal_cdf(z) - p) / normal_pdf(z);
+    z -= dz;
+    if (std::fabs(dz) < 1e-16 * (1.0 + std::fabs(z))) break;
+  }
+  return z;
+}
+
+nf4k::Codebook make_codebook() {
+  const double d = 0.5 * (1.0 / 32.0 + 1.0 / 30.0);
+  double v[16];
+  int n = 0;
+  for (int j = 0; j < 8; ++j) v[n++] = normal_quantile(1.0 - d - j * (0.5 - d) / 8.0);
+  for (int j = 0; j < 7; ++j) v[n++] = normal_quantile(d + j * (0.5 - d) / 7.0);
+  v[n++] = 0.0;
+  const double top = normal_quantile(1.0 - d);
+  for (double& e : v) e /= top;
+  for (int i = 1; i < 16; ++i)
+    for (int j = i; j > 0 && v[j - 1] > v[j]; --j) std::swap(v[j - 1], v[j]);
+  nf4k::Codebook cb;
+  for (int i = 0; i < 16; ++i) cb.v[i] = (float)v[i];
+  return cb;
+}
+
+const nf4k::Codebook& codebook() {
+  static const nf4k::Codebook cb = make_codebook();
+  return cb;
+}
+
+// ------------------------------------------------------------------ device
+
+struct DeviceInfo {
+  int checked = 0;
+  int cc_major = 0, cc_minor = 0, sms = 0;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+nf4_status current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return fail(NF4_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (*dev < 0 || *dev >= 64) return fail(NF4_ECUDA, "device ordinal %d out of range", *dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[*dev];
+  if (!d.checked) {
+    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, *dev);
+    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, *dev);
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(NF4_ECUDA, "device query: %s", cudaGetErrorString(e));
+    d.checked = 1;
+  }
+  if (!(d.cc_major == 10 && d.cc_minor == 3))
+    return fail(NF4_EARCH, "device %d is sm_%d%d; libnf4 is built for sm_103a only", *dev, d.cc_major,
+                d.cc_minor);
+  return NF4_OK;
+}
+
+// -------------------------------------------------------------- validation
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+nf4_status check_shape(int64_t M, int64_t K, const char* what) {
+  if (M < 1 || M >= (int64_t(1) << 31))
+    return fail(NF4_EINVAL, "%s: M = %lld must be in [1, 2^31)", what, (long long)M);
+  if (K < 64 || K % 64 != 0 || K > NF4_MAX_K)
+    return fail(NF4_EINVAL, "%s: K = %lld must be a positive multiple of 64 and <= %d", what, (long long)K,
+                NF4_MAX_K);
+  return NF4_OK;
+}
+
+nf4_status check_weight(const nf4_weight* W, const char* what) {
+  if (!W) return fail(NF4_ENULL, "%s: weight descriptor is NULL", what);
+  nf4_status st = check_shape(W->M, W->K, what);
+  if (st) return st;
+  if (!W->codes || !W->scales) return fail(NF4_ENULL, "%s: codes or scales is NULL", what);
+  if (!aligned(W->codes, 16)) return fail(NF4_EALIGN, "%s: codes must be 16-byte aligned", what);
+  if (!aligned(W->scales, 4)) return fail(NF4_EALIGN, "%s: scales must be 4-byte aligned", what);
+  return NF4_OK;
+}
+
+nf4_status check_x(const void* x, nf4_dtype xt, const char* what) {
+  if (!x) return fail(NF4_ENULL, "%s: x is NULL", what);
+  if (xt != NF4_F32 && xt != NF4_BF16) return fail(NF4_EINVAL, "%s: unknown activation dtype %d", what, (int)xt);
+  if (!aligned(x, 16)) return fail(NF4_EALIGN, "%s: x must be 16-byte aligned", what);
+  return NF4_OK;
+}
+
+nf4_status check_out(const void* p, size_t align, const char* name, const char* what) {
+  if (!p) return fail(NF4_ENULL, "%s: %s is NULL", what, name);
+  if (!aligned(p, align)) return fail(NF4_EALIGN, "%s: %s must be %zu-byte aligned", what, name, align);
+  return NF4_OK;
+}
+
+nf4_status launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(NF4_ECUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  return NF4_OK;
+}
+
+nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const void* x, nf4_dtype xt,
+                    const float* resid, float* y, uint16_t* out, int64_t* index, void* ws, nf4_stream stream,
+                    const char* what) {
+  int dev = 0;
+  nf4_status st = current_device(&dev);
+  if (st) return st;
+  nf4k::GemvArgs a{};
+  a.codes = W->codes;
+  a.scales = W->scales;
+  if (W2) {
+    a.codes2 = W2->codes;
+    a.scales2 = W2->scales;
+  }
+  a.x = x;
+  a.resid = resid;
+  a.y = y;
+  a.out_bf16 = out;
+  a.index = index;
+  a.ws = reinterpret_cast<unsigned long long*>(ws);
+  a.M = (int)W->M;
+  a.K = (int)W->K;
+  a.cb = codebook();
+  const nf4k::GemvConfig cfg = nf4k::choose_gemv_config(epi, W->M, W->K, dev);
+  a.G = cfg.G;
+  a.gpc = cfg.gpc;
+  return launched(nf4k::launch_gemv(epi, xt == NF4_BF16, a, cfg, reinterpret_cast<cudaStream_t>(stream)), what);
+}
+
+}  // namespace
+
+extern "C" {
+
+nf4_status nf4_gemv(const nf4_weight* W, const void* x, nf4_dtype xt, float* y, nf4_stream stream) {
+  const char* what = "nf4_gemv";
+  nf4_status st;
+  if ((st = check_weight(W, what)) || (st = check_x(x, xt, what)) || (st = check_out(y, 4, "y", what))) return st;
+  return run_gemv(nf4k::EPI_PLAIN, W, nullptr, x, xt, nullptr, y, nullptr, nullptr, nullptr, stream, what);
+}
+
+nf4_status nf4_gemv_residual(const nf4_weight* W, const void* x, nf4_dtype xt, const float* residual, float* y,
+                             nf4_stream stream) {
+  const char* what = "nf4_gemv_residual";
+  nf4_status st;
+  if ((st = check_weight(W, what)) || (st = check_x(x, xt, what)) || (st = check_out(y, 4, "y", what)) ||
+      (st = check_out(residual, 4, "residual", what)))
+    return st;
+  return run_gemv(nf4k::EPI_RESID, W, nullptr, x, xt, residual, y, nullptr, nullptr, nullptr, stream, what);
+}
+
+nf4_status nf4_gemv_swiglu(const nf4_weight* Wg, const nf4_weight* Wu, const void* x, nf4_dtype xt, uint16_t* out,
+                           nf4_stream stream) {
+  const char* what = "nf4_gemv_swiglu";
+  nf4_status st;
+  if ((st = check_weight(Wg, what)) || (st = check_weight(Wu, what)) || (st = check_x(x, xt, what)) ||
+      (st = check_out(out, 2, "out", what)))
+    return st;
+  if (Wg->M != Wu->M || Wg->K != Wu->K)
+    return fail(NF4_EINVAL, "%s: gate is %lldx%lld but up is %lldx%lld", what, (long long)Wg->M,
+                (long long)Wg->K, (long long)Wu->M, (long long)Wu->K);
+  return run_gemv(nf4k::EPI_SWIGLU, Wg, Wu, x, xt, nullptr, nullptr, out, nullptr, nullptr, stream, what);
+}
+
+nf4_status nf4_gemv_argmax(const nf4_weight* W, const void* x, nf4_dtype xt, float* logits, int64_t* index,
+                           void* workspace, nf4_stream stream) {
+  const char* what = "nf4_gemv_argmax";
+  nf4_status st;
+  if ((st = check_weight(W, what)) || (st = check_x(x, xt, what)) || (st = check_out(logits, 4, "logits", what)) ||
+      (st = check_out(index, 8, "index", what)) || (st = check_out(workspace, 8, "workspace", what)))
+    return st;
+  return run_gemv(nf4k::EPI_ARGMAX, W, nullptr, x, xt, nullptr, logits, nullptr, index, workspace, stream, what);
+}
+
+nf4_status nf4_gemm_chunk(const nf4_weight* W, const uint16_t* X, int N, float* Y, void* workspace,
+                          nf4_stream stream) {
+  const char* what = "nf4_gemm_chunk";
+  nf4_status st;
+  if ((st = check_weight(W, what))) return st;
+  if (N < 1 || N > NF4_MAX_CHUNK_N) return fail(NF4_EINVAL, "%s: N = %d must be in [1, %d]", what, N, NF4_MAX_CHUNK_N);
+  if ((st = check_out(X, 16, "X", what)) || (st = check_out(Y, 4, "Y", what))) return st;
+  const size_t need = nf4_workspace_bytes(W->M, W->K, N);
+  if (need && (st = check_out(workspace, 16, "workspace", what))) return st;
+  int dev = 0;
+  if ((st = current_device(&dev))) return st;
+  return launched(nf4k::launch_chunk(W->codes, W->scales, (int)W->M, (int)W->K, X, N, Y, workspace, codebook(),
+                                     reinterpret_cast<cudaStream_t>(stream), dev),
+                  what);
+}
+
+size_t nf4_workspace_bytes(int64_t M, int64_t K, int N) {
+  if (M < 1 || K < 64 || K % 64 || N < 1 || N > NF4_MAX_CHUNK_N) return 0;
+  if (N == 1) return 16;  // argmax: 64-bit key + block ticket
+  return nf4k::chunk_workspace_bytes(M, K, N);
+}
+
+nf4_status nf4_quantize(const float* W, int64_t M, int64_t K, uint8_t* codes, float* scales, nf4_stream stream) {
+  const char* what = "nf4_quantize";
+  nf4_status st;
+  if ((st = check_shape(M, K, what))) return st;
+  if ((st = check_out(W, 16, "W", what)) || (st = check_out(codes, 16, "codes", what)) ||
+      (st = check_out(scales, 4, "scales", what)))
+    return st;
+  int dev = 0;
+  if ((st = current_device(&dev))) return st;
+  return launched(nf4k::launch_quantize(W, M, K, codes, scales, codebook(), reinterpret_cast<cudaStream_t>(stream), dev),
+                  what);
+}
+
+void nf4_codebook(float out[16]) {
+  const nf4k::Codebook& cb = codebook();
+  for (int i = 0; i < 16; ++i) out[i] = cb.v[i];
+}
+
+const char* nf4_last_error(void) { return g_last_error.c_str(); }
+
+const char* nf4_describe_config(int64_t M, int64_t K, int N) {
+  if (check_shape(M, K, "nf4_describe_config") || N < 1 || N > NF4_MAX_CHUNK_N) {
+    g_describe = std::string("invalid shape: ") + g_last_error;
+    return g_describe.c_str();
+  }
+  int dev = 0;
+  if (current_device(&dev)) {
+    g_describe = std::string("no usable device: ") + g_last_error;
+    return g_describe.c_str();
+  }
+  char buf[512];
+  if (N == 1) {
+    const nf4k::GemvConfig c = nf4k::choose_gemv_config(nf4k::EPI_PLAIN, M, K, dev);
+    std::snprintf(buf, sizeof buf,
+                  "gemv M=%lld K=%lld: %d thread(s) per row (%d chunk(s) of 32 weights each), %d row(s) per "
+                  "batch, %d row group(s) per block, %d blocks of %d threads, %d B shared memory%s",
+                  (long long)M, (long long)K, c.G, c.nch, c.rb, c.gpc, c.blocks, c.G * c.gpc, c.smem,
+                  c.big ? ", register-capped" : "");
+  } else {
+    std::snprintf(buf, sizeof buf, "%s", nf4k::describe_chunk(M, K, N, dev).c_str());
+  }
+  g_describe = buf;
+  return g_describe.c_str();
+}
+
+}  // extern "C"

@@ -1,0 +1,136 @@
+// gemv_host.cu -- per-shape configuration and launch of the N=1 kernels.
+//
+// The configuration table follows the source page's rule "pick by (M, K)
+// microbench" ("Decode V2 -- resident executor", section 6): the page packs
+// NR = 4 rows per block for M >= 4096 and keeps one row for M = 2048 on a
+// 70-SM desktop part.  Here the equivalents are the row-group width G (threads
+// sharing one row, set by K), the batch RB (rows in flight per thread) and the
+// number of groups per block, with the grid sized to fill all SMs once
+// (persistent blocks, each owning a contiguous range of rows).
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "gemv_dispatch.cuh"
+
+namespace nf4k {
+
+namespace {
+
+const void* kernel_ptr(int epi, int nch, int rb, bool big, bool xb) {
+  switch (epi) {
+    case EPI_PLAIN: return GemvDispatch<EPI_PLAIN>::ptr(nch, rb, big, xb);
+    case EPI_RESID: return GemvDispatch<EPI_RESID>::ptr(nch, rb, big, xb);
+    case EPI_SWIGLU: return GemvDispatch<EPI_SWIGLU>::ptr(nch, rb, big, xb);
+    default: return GemvDispatch<EPI_ARGMAX>::ptr(nch, rb, big, xb);
+  }
+}
+
+// Largest block the instantiation can launch (its register use decides).
+int max_threads(int epi, int nch, int rb, bool big) {
+  int m = 1 << 30;
+  for (int xb = 0; xb < 2; ++xb) {
+    cudaFuncAttributes attr{};
+    if (cudaFuncGetAttributes(&attr, kernel_ptr(epi, nch, rb, big, xb != 0)) != cudaSuccess) return 0;
+    m = attr.maxThreadsPerBlock < m ? attr.maxThreadsPerBlock : m;
+  }
+  return m;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  return (v && *v) ? std::atoi(v) : dflt;
+}
+
+struct Key {
+  int epi, device;
+  int64_t M, K;
+  bool operator<(const Key& o) const {
+    return std::tie(epi, device, M, K) < std::tie(o.epi, o.device, o.M, o.K);
+  }
+};
+
+std::mutex g_mu;
+std::map<Key, GemvConfig> g_cache;
+
+}  // namespace
+
+GemvConfig choose_gemv_config(int epi, int64_t M, int64_t K, int device) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_cache.find(Key{epi, device, M, K});
+    if (it != g_cache.end()) return it->second;
+  }
+  GemvConfig c{};
+  const bool two = (epi == EPI_SWIGLU);
+  const int H = (int)(K / 32);            // 16-byte code chunks per row
+  const int G1 = 32 * ((H + 31) / 32);    // group width with one chunk per thread
+  const int G2 = 32 * ((H + 63) / 64);    // group width with two chunks per thread
+  // candidates in order of preference: (nch, rb, big)
+  const int cand[][3] = {
+      {H <= 32 ? 1 : (H <= 64 ? 2 : 1), two ? 2 : 4, 0},
+      {1, 2, 0}, {2, 2, 0}, {1, 2, 1}, {2, 2, 1}};
+  int pick = -1, mt = 0;
+  for (int i = 0; i < 5 && pick < 0; ++i) {
+    int nch = cand[i][0], rb = cand[i][1];
+    const bool big = cand[i][2] != 0;
+    if (i == 0) rb = env_int("NF4_GEMV_RB", rb);
+    if (!gemv_variant_exists(nch, rb, big)) continue;
+    const int G = (H <= 32) ? 32 : (nch == 1 ? G1 : G2);
+    const int m = max_threads(epi, nch, rb, big);
+    if (G <= m && G <= 1024) {
+      pick = i;
+      c.nch = nch;
+      c.rb = rb;
+      c.big = big;
+      c.G = G;
+      mt = m;
+    }
+  }
+  if (pick < 0) {  // cannot happen for K <= 65536: (2, 2, big) needs G2 <= 1024
+    c.blocks = 0;
+    return c;
+  }
+  int gpc = mt / c.G;
+  gpc = gpc < 1 ? 1 : gpc;
+  const int gpc_cap = (c.G == 32) ? 32 : 15;  // named barrier ids 1..15
+  gpc = gpc > gpc_cap ? gpc_cap : gpc;
+  gpc = env_int("NF4_GEMV_GPC", gpc);
+  if (gpc * c.G > mt) gpc = mt / c.G;
+  if (gpc > gpc_cap) gpc = gpc_cap;
+  if (gpc < 1) gpc = 1;
+  const int nv = two ? 2 : 1;
+  c.gpc = gpc;
+  c.smem = LUT_BYTES + gpc * 2 * nv * c.rb * (c.G / 32) * (int)sizeof(float);
+
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  for (int xb = 0; xb < 2; ++xb)
+    cudaFuncSetAttribute(kernel_ptr(epi, c.nch, c.rb, c.big, xb != 0), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         c.smem);
+  int bps = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kernel_ptr(epi, c.nch, c.rb, c.big, true), c.G * c.gpc,
+                                                c.smem);
+  bps = bps < 1 ? 1 : bps;
+  bps = env_int("NF4_GEMV_BPS", bps);
+  const int64_t want = (M + c.gpc - 1) / c.gpc;
+  const int64_t have = (int64_t)(sms > 0 ? sms : 1) * bps;
+  c.blocks = (int)(want < have ? want : have);
+  cudaGetLastError();  // attribute queries leave no sticky state behind
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_cache[Key{epi, device, M, K}] = c;
+  return c;
+}
+
+cudaError_t launch_gemv(int epi, bool xb, const GemvArgs& a, GemvConfig cfg, cudaStream_t s) {
+  if (cfg.blocks < 1) return cudaErrorInvalidConfiguration;
+  switch (epi) {
+    case EPI_PLAIN: return GemvDispatch<EPI_PLAIN>::launch(cfg.nch, cfg.rb, cfg.big, xb, a, cfg, s);
+    case EPI_RESID: return GemvDispatch<EPI_RESID>::launch(cfg.nch, cfg.rb, cfg.big, xb, a, cfg, s);
+    case EPI_SWIGLU: return GemvDispatch<EPI_SWIGLU>::launch(cfg.nch, cfg.rb, cfg.big, xb, a, cfg, s);
+    default: return GemvDispatch<EPI_ARGMAX>::launch(cfg.nch, cfg.rb, cfg.big, xb, a, cfg, s);
+  }
+}
+
+}  // namespace nf4k

@@ -1,0 +1,305 @@
+"""GPU parity of the N=1 path (nf4_gemv / _residual / _swiglu / _argmax) and of
+the device encoder against the CPU oracle, through the C ABI.
+
+Sizes: small cases spanning several blocks and ragged tails for every branch of
+the per-shape configuration, plus the full-size workloads (3B down+residual,
+3B SwiGLU, 3B lm_head+argmax, 14B N=1) compared on every row.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from nf4_weight_quantized_gb300 import synth
+
+from . import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+# Worst-case relative fp32 error of the kernel's fixed summation tree (at most
+# ~50 sequential roundings per output, plus the two of cb*x and the scale):
+# used only to decide whether a seed's argmax is well-posed, never as the
+# pass/fail tolerance.
+KERNEL_REL = 64 * 2.0 ** -24
+
+
+@pytest.fixture(scope="module")
+def nf4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from nf4_weight_quantized_gb300 import nf4 as mod
+
+    return mod
+
+
+# --------------------------------------------------------------- encoder
+
+def test_quantize_bitexact_special_blocks(nf4):
+    cb = oracle.codebook()
+    W = synth.weights(30, 0, 16, 512)
+    W[0, :64] = 0.0                       # zero block
+    W[0, 64:128] = -0.0                   # negative zeros
+    W[1, :64] = 1e-40                     # subnormal, equal values
+    W[2, :64] = np.linspace(-3e30, 3e30, 64, dtype=np.float32)
+    W[3, :64] = 0.0
+    W[3, 0] = 1.0                         # exact midpoints of the table, absmax 1
+    for i in range(15):
+        W[3, 1 + i] = np.float32((float(cb[i]) + float(cb[i + 1])) / 2)
+    W[4, :64] = -W[4, :64]
+    codes, scales = oracle.quantize(W)
+    Wt = torch.from_numpy(W).cuda()
+    q = nf4.nf4_quantize(Wt)
+    torch.cuda.synchronize()
+    assert np.array_equal(q.codes.cpu().numpy(), codes)
+    assert np.array_equal(q.scales.cpu().numpy().view(np.uint32), scales.view(np.uint32))
+
+
+def test_quantize_bitexact_full_down_shape(nf4):
+    W = synth.weights(1, 0, 2048, 11008)
+    codes, scales = oracle.quantize(W)
+    q = nf4.nf4_quantize(torch.from_numpy(W).cuda())
+    assert np.array_equal(q.codes.cpu().numpy(), codes)
+    assert np.array_equal(q.scales.cpu().numpy(), scales)
+
+
+# ------------------------------------------------------------------ gemv
+
+# (M, K) chosen to reach every configuration branch: one or two 32-weight
+# chunks per thread, one warp or many per row, ragged chunk counts, K = 64
+# and the largest K.
+SHAPES = [(1, 64), (2, 64), (31, 128), (33, 1024), (7, 1088), (65, 2048), (33, 2112), (19, 5120),
+          (2049, 11008), (3, 32768), (5, 32832), (2, 65536), (1000, 256)]
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+@pytest.mark.parametrize("xd", ["f32", "bf16"])
+def test_gemv_shapes(nf4, M, K, xd):
+    seed = 100 + M + K
+    codes, scales = H.quantized(seed, 0, M, K)
+    x = H.make_x(seed, K, xd)
+    y_ref, S = oracle.gemv(codes, scales, x)
+    W = H.weight_tensors(codes, scales)
+    y = torch.full((M + 64,), 12345.0, device="cuda")  # guard band after the output
+    nf4.nf4_gemv(W, H.x_tensor(x), y[:M])
+    yh = y.cpu().numpy()
+    H.assert_within(yh[:M], y_ref, S, what=f"gemv {M}x{K} {xd}")
+    assert np.all(yh[M:] == 12345.0), "wrote past the output"
+
+
+def test_gemv_tiny_workload(nf4):
+    w = synth.WORKLOADS["tiny"]
+    d = synth.workload_inputs(w)
+    codes, scales = oracle.quantize(d["W"])
+    y_ref, S = oracle.gemv(codes, scales, d["x"])
+    y = nf4.nf4_gemv(H.weight_tensors(codes, scales), H.x_tensor(d["x"]))
+    rel = H.assert_within(y.cpu().numpy(), y_ref, S, what="tiny")
+    assert rel < 1e-5  # fp32 accumulation is far inside the stated bound
+
+
+def test_gemv_deterministic_and_position_independent(nf4):
+    M, K = 3000, 2048
+    codes, scales = H.quantized(41, 0, M, K)
+    codes[2999] = codes[7]
+    scales[2999] = scales[7]
+    codes[1500] = codes[7]
+    scales[1500] = scales[7]
+    x = H.x_tensor(H.make_x(41, K, "bf16"))
+    W = H.weight_tensors(codes, scales)
+    y1 = nf4.nf4_gemv(W, x).cpu().numpy()
+    y2 = nf4.nf4_gemv(W, x).cpu().numpy()
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    assert y1[7] == y1[1500] == y1[2999]
+
+
+def test_zero_level_rows_exact(nf4):
+    M, K = 40, 2048
+    codes = np.full((M, K // 2), 0x77, np.uint8)
+    g = np.random.Generator(np.random.PCG64(42))
+    scales = (g.standard_normal((M, K // 64)) * 50).astype(np.float32)
+    W = H.weight_tensors(codes, scales)
+    x = H.x_tensor(H.make_x(42, K, "bf16"))
+    y = nf4.nf4_gemv(W, x).cpu().numpy()
+    assert np.all(y == 0.0)
+    r = torch.from_numpy(g.standard_normal(M).astype(np.float32)).cuda()
+    yr = nf4.nf4_gemv_residual(W, x, r)
+    assert torch.equal(yr, r)
+
+
+def test_gemv_on_side_stream_and_graph(nf4):
+    M, K = 2048, 11008
+    codes, scales = H.quantized(43, 0, M, K)
+    W = H.weight_tensors(codes, scales)
+    x = H.x_tensor(H.make_x(43, K, "bf16"))
+    r = torch.randn(M, device="cuda")
+    eager = nf4.nf4_gemv_residual(W, x, r)
+    s = torch.cuda.Stream()
+    y = torch.empty(M, device="cuda")
+    with torch.cuda.stream(s):
+        nf4.nf4_gemv_residual(W, x, r, y, stream=s)
+    s.synchronize()
+    assert torch.equal(y, eager)
+    y.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        nf4.nf4_gemv_residual(W, x, r, y)
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(20):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, eager)
+    assert torch.cuda.mem_get_info()[0] == free0  # no device allocation per call
+
+
+# -------------------------------------------------------------- residual
+
+@pytest.mark.parametrize("M,K", [(1, 64), (37, 2048), (2048, 11008)])
+def test_residual(nf4, M, K):
+    seed = 200 + M
+    codes, scales = H.quantized(seed, 0, M, K)
+    x = H.make_x(seed, K, "bf16")
+    r = synth.normal_f32(seed, 3, M)
+    y64, _ = oracle.gemv_residual(codes, scales, x, r)
+    _, S = oracle.gemv(codes, scales, x)
+    W = H.weight_tensors(codes, scales)
+    rt = torch.from_numpy(r).cuda()
+    y = nf4.nf4_gemv_residual(W, H.x_tensor(x), rt).cpu().numpy()
+    H.assert_within(y, y64, S, extra=H.ulp_f32(y64), what="residual")
+    # in place: y aliases the residual
+    rt2 = rt.clone()
+    nf4.nf4_gemv_residual(W, H.x_tensor(x), rt2, rt2)
+    assert np.array_equal(rt2.cpu().numpy(), y)
+
+
+def test_down_residual_full(nf4):
+    w = synth.WORKLOADS["down_residual"]
+    d = synth.workload_inputs(w)
+    codes, scales = oracle.quantize(d["W"])
+    y64, _ = oracle.gemv_residual(codes, scales, d["x"], d["r"])
+    _, S = oracle.gemv(codes, scales, d["x"])
+    y = nf4.nf4_gemv_residual(H.weight_tensors(codes, scales), H.x_tensor(d["x"]),
+                              torch.from_numpy(d["r"]).cuda()).cpu().numpy()
+    rel = H.assert_within(y, y64, S, extra=H.ulp_f32(y64), what="down_residual")
+    assert rel < 1e-5
+
+
+# ---------------------------------------------------------------- swiglu
+
+def _check_swiglu(nf4, gc, gs, uc, us, x, what):
+    o64, _, g, u = oracle.gemv_swiglu(gc, gs, uc, us, x)
+    _, Sg = oracle.gemv(gc, gs, x)
+    _, Su = oracle.gemv(uc, us, x)
+    out = nf4.nf4_gemv_swiglu(H.weight_tensors(gc, gs), H.weight_tensors(uc, us), H.x_tensor(x))
+    ob = H.bf16_bits_of(out)
+    of = synth.bf16_to_f32(ob).astype(np.float64)
+    bound = H.swiglu_bound(g, u, Sg, Su) + H.ulp_bf16(o64)
+    err = np.abs(of - o64)
+    bad = np.nonzero(~(err <= bound))[0]
+    assert bad.size == 0, f"{what}: rows {bad[:5]} err {err[bad[:5]]} bound {bound[bad[:5]]}"
+    return ob, oracle.gemv_swiglu(gc, gs, uc, us, x)[1]
+
+
+@pytest.mark.parametrize("M,K", [(1, 64), (45, 2048), (300, 5120), (70, 11008)])
+def test_swiglu_shapes(nf4, M, K):
+    seed = 300 + M
+    gc, gs = H.quantized(seed, 0, M, K)
+    uc, us = H.quantized(seed, 1, M, K)
+    _check_swiglu(nf4, gc, gs, uc, us, H.make_x(seed, K, "bf16"), f"swiglu {M}x{K}")
+
+
+def test_swiglu_full(nf4):
+    w = synth.WORKLOADS["swiglu"]
+    d = synth.workload_inputs(w)
+    gc, gs = oracle.quantize(d["W"])
+    uc, us = oracle.quantize(d["Wu"])
+    ob, ref_bits = _check_swiglu(nf4, gc, gs, uc, us, d["x"], "swiglu full")
+    # fp32 silu(g)*u rounds to the same bf16 as the float64 value on almost every row
+    assert np.mean(ob == ref_bits) > 0.99
+
+
+# ---------------------------------------------------------------- argmax
+
+def _argmax_check(nf4, codes, scales, x, ws=None):
+    l64, _, idx_ref = oracle.gemv_argmax(codes, scales, x)
+    _, S = oracle.gemv(codes, scales, x)
+    W = H.weight_tensors(codes, scales)
+    logits, index = nf4.nf4_gemv_argmax(W, H.x_tensor(x), workspace=ws)
+    lg = logits.cpu().numpy()
+    H.assert_within(lg, l64, S, what="logits")
+    gi = int(index.cpu().item())
+    assert gi == int(np.argmax(lg)), "index is not the argmax of the kernel's own logits"
+    gap = H.top2_gap(l64)
+    if gap > 2 * KERNEL_REL * float(np.max(S)):
+        assert gi == idx_ref, f"index {gi} != oracle {idx_ref} (gap {gap})"
+    return gi, idx_ref, lg
+
+
+@pytest.mark.parametrize("M,K", [(1, 64), (2, 128), (1000, 2048), (5000, 5120)])
+def test_argmax_shapes(nf4, M, K):
+    seed = 400 + M
+    codes, scales = H.quantized(seed, 0, M, K)
+    _argmax_check(nf4, codes, scales, H.make_x(seed, K, "bf16"))
+
+
+def test_argmax_ties_go_to_lowest_index(nf4):
+    M, K = 20000, 2048
+    codes, scales = H.quantized(44, 0, M, K)
+    x = H.make_x(44, K, "bf16")
+    _, _, best = oracle.gemv_argmax(codes, scales, x)
+    for lo in (best // 3, 0):
+        c2, s2 = codes.copy(), scales.copy()
+        for r in (lo, M - 1, (best + M) // 2):
+            c2[r], s2[r] = codes[best], scales[best]
+        gi, ir, lg = _argmax_check(nf4, c2, s2, x)
+        assert gi == ir == min(lo, best)
+        assert lg[lo] == lg[best] == lg[M - 1]
+
+
+def test_argmax_all_equal_and_workspace_reuse(nf4):
+    M, K = 4096, 2048
+    codes = np.full((M, K // 2), 0x77, np.uint8)
+    scales = np.ones((M, K // 64), np.float32)
+    ws = nf4.new_workspace(M, K)
+    x = H.make_x(45, K, "bf16")
+    gi, ir, _ = _argmax_check(nf4, codes, scales, x, ws)
+    assert gi == ir == 0
+    # the workspace is left zeroed; a different problem through the same workspace
+    assert torch.count_nonzero(ws).item() == 0
+    codes2, scales2 = H.quantized(45, 0, M, K)
+    for seed in (46, 47, 48):
+        gi, ir, _ = _argmax_check(nf4, codes2, scales2, H.make_x(seed, K, "bf16"), ws)
+        assert gi == ir
+    assert torch.count_nonzero(ws).item() == 0
+
+
+def test_lm_head_argmax_full(nf4):
+    w = synth.WORKLOADS["lm_head_argmax"]
+    d = synth.workload_inputs(w)
+    codes, scales = oracle.quantize(d["W"])
+    gi, ir, _ = _argmax_check(nf4, codes, scales, d["x"])
+    assert gi == ir
+
+
+def test_gemv14b_full(nf4):
+    w = synth.WORKLOADS["gemv14b"]
+    d = synth.workload_inputs(w)
+    codes, scales = oracle.quantize(d["W"])
+    y_ref, S = oracle.gemv(codes, scales, d["x"])
+    y = nf4.nf4_gemv(H.weight_tensors(codes, scales), H.x_tensor(d["x"])).cpu().numpy()
+    H.assert_within(y, y_ref, S, what="gemv14b")
+
+
+# ---------------------------------------------------------------- errors
+
+def test_errors_are_raised(nf4):
+    codes, scales = H.quantized(49, 0, 4, 128)
+    W = H.weight_tensors(codes, scales)
+    x = torch.zeros(129, device="cuda")
+    with pytest.raises(nf4.NF4Error) as e:
+        nf4.nf4_gemv(W, x[1:])  # data pointer 4 bytes past a 16-byte boundary
+    assert e.value.status == -2
+    bad = nf4.NF4Weight(W.codes[:, :48].contiguous(), W.scales[:, :1].contiguous().repeat(1, 1))
+    with pytest.raises(nf4.NF4Error) as e:
+        nf4.nf4_gemv(bad, torch.zeros(96, device="cuda"))
+    assert e.value.status == -1
