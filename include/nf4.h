@@ -72,7 +72,8 @@ typedef enum nf4_status {
   NF4_EALIGN = -2, /* a pointer is not aligned as stated above */
   NF4_ENULL = -3,  /* a required pointer is NULL */
   NF4_ECUDA = -4,  /* a CUDA runtime call or launch failed; see nf4_last_error() */
-  NF4_EARCH = -5   /* the current device is not compute capability 10.3 (sm_103a) */
+  NF4_EARCH = -5,  /* the current device is not compute capability 10.3 (sm_103a) */
+  NF4_ETIMEOUT = -6 /* a kernel's bounded wait ran out (nf4_check_device_errors only) */
 } nf4_status;
 
 /* Activation element type. */
@@ -157,6 +158,17 @@ size_t nf4_workspace_bytes(int64_t M, int64_t K, int N);
  */
 nf4_status nf4_quantize(const float* W, int64_t M, int64_t K, uint8_t* codes, float* scales,
                         nf4_stream stream);
+
+/*
+ * Diagnostic, not for the hot path: synchronizes the current device, then
+ * reads and clears the library's device-side error words.  Kernels that wait
+ * on shared-memory barriers (bulk-copy pipelines, tensor-core commits) bound
+ * every wait; a wait that runs out (which needs a broken device or library)
+ * makes the block skip its remaining work and sets an error word instead of
+ * hanging.  Returns NF4_ETIMEOUT if that happened since the last check (the
+ * outputs of the calls in between are invalid), NF4_OK otherwise.
+ */
+nf4_status nf4_check_device_errors(void);
 
 /* Host copy of the 16 fp32 codebook levels the kernels use. Never fails. */
 void nf4_codebook(float out[16]);

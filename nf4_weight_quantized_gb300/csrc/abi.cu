@@ -3,9 +3,11 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "common.cuh"
 #include "nf4.h"
@@ -67,6 +69,17 @@ nf4k::Codebook make_codebook() {
 const nf4k::Codebook& codebook() {
   static const nf4k::Codebook cb = make_codebook();
   return cb;
+}
+
+// ------------------------------------------------- device error registry
+
+std::mutex& readers_mu() {
+  static std::mutex mu;
+  return mu;
+}
+std::vector<nf4k::DeviceErrorReader>& readers() {
+  static std::vector<nf4k::DeviceErrorReader> v;
+  return v;
 }
 
 // ------------------------------------------------------------------ device
@@ -139,6 +152,15 @@ nf4_status launched(cudaError_t e, const char* what) {
   return NF4_OK;
 }
 
+// NF4_GEMV_KERNEL=register forces the register-prefetch kernel (tuning runs).
+bool use_register_kernel() {
+  static const bool v = [] {
+    const char* e = std::getenv("NF4_GEMV_KERNEL");
+    return e && std::strcmp(e, "register") == 0;
+  }();
+  return v;
+}
+
 nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const void* x, nf4_dtype xt,
                     const float* resid, float* y, uint16_t* out, int64_t* index, void* ws, nf4_stream stream,
                     const char* what) {
@@ -161,6 +183,16 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
   a.M = (int)W->M;
   a.K = (int)W->K;
   a.cb = codebook();
+  const bool scales16 = aligned(W->scales, 16) && (!W2 || aligned(W2->scales, 16));
+  if (scales16 && !use_register_kernel()) {
+    const nf4k::TmaConfig tc = nf4k::choose_tma_config(epi, W->M, W->K, dev);
+    if (tc.ok) {
+      a.G = tc.G;
+      a.gpc = tc.gpc;
+      return launched(nf4k::launch_gemv_tma(epi, xt == NF4_BF16, a, tc, reinterpret_cast<cudaStream_t>(stream)),
+                      what);
+    }
+  }
   const nf4k::GemvConfig cfg = nf4k::choose_gemv_config(epi, W->M, W->K, dev);
   a.G = cfg.G;
   a.gpc = cfg.gpc;
@@ -169,7 +201,31 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
 
 }  // namespace
 
+namespace nf4k {
+void register_device_error_reader(DeviceErrorReader f) {
+  std::lock_guard<std::mutex> lk(readers_mu());
+  readers().push_back(f);
+}
+}  // namespace nf4k
+
 extern "C" {
+
+nf4_status nf4_check_device_errors(void) {
+  int dev = 0;
+  nf4_status st = current_device(&dev);
+  if (st) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(NF4_ECUDA, "nf4_check_device_errors: %s", cudaGetErrorString(e));
+  unsigned int bits = 0;
+  {
+    std::lock_guard<std::mutex> lk(readers_mu());
+    for (auto f : readers()) bits |= f();
+  }
+  if (bits & nf4k::kErrWaitTimeout)
+    return fail(NF4_ETIMEOUT, "a kernel gave up waiting on a shared-memory barrier; its outputs are invalid");
+  return NF4_OK;
+}
+
 
 nf4_status nf4_gemv(const nf4_weight* W, const void* x, nf4_dtype xt, float* y, nf4_stream stream) {
   const char* what = "nf4_gemv";

@@ -41,6 +41,122 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// ---- shared-memory barriers and bulk copies (sm_90+ async proxy) ----------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make initialized barriers visible to the async proxy (bulk copies, MMA).
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Upper bound on polls of one barrier phase (each poll may itself block for a
+// short hardware-defined time); past it the kernel gives up (see WaitGuard).
+constexpr uint32_t kWaitPolls = 1u << 22;
+
+// Error word set by kernels whose bounded waits ran out (0 = none).  Device
+// code is compiled per translation unit (no relocatable device linking), so
+// every unit that includes this header has its own word; a static initializer
+// registers the unit's reader with the library (nf4_check_device_errors).
+static __device__ unsigned int g_nf4_device_error;
+constexpr unsigned int kErrWaitTimeout = 1u;
+
+using DeviceErrorReader = unsigned int (*)();
+void register_device_error_reader(DeviceErrorReader f);  // abi.cu
+
+namespace {
+// Reads and clears this unit's error word on the current device (synchronous).
+unsigned int read_and_clear_device_error() {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_nf4_device_error, sizeof v) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (v) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_nf4_device_error, &z, sizeof z);
+  }
+  return v;
+}
+struct DeviceErrorRegistration {
+  DeviceErrorRegistration() { register_device_error_reader(&read_and_clear_device_error); }
+};
+const DeviceErrorRegistration g_device_error_registration;
+}  // namespace
+
+// Bounded wait on one barrier phase.  `abort` is a block-shared flag: once any
+// wait in the block has timed out, later waits return at once, so the block
+// runs to its end (keeping every block-level barrier matched) without hanging.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+  }
+  *abort = 1;
+  atomicOr(&g_nf4_device_error, kErrWaitTimeout);
+  return false;
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` on the barrier's tx count.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for data read exactly once (weights): evict first.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// d0 += a0 * b0, d1 += a1 * b1 with one packed fp32x2 FMA (sm_100+).
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%0, %1};\n\t"
+      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -78,6 +194,15 @@ struct GemvConfig {
   int blocks;   // grid size
   int smem;     // dynamic shared memory bytes
 };
+
+// Bulk-copy (TMA-engine) N=1 configuration (gemv_host.cu).
+struct TmaConfig {
+  bool ok;       // the shape and alignment allow the bulk-copy kernel
+  int nch, rb, lut, G, gpc, blocks, threads, smem;
+  int SR, S, stage_bytes, codes_bytes, scales_bytes, bar_off, red_off;
+};
+TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device);
+cudaError_t launch_gemv_tma(int epi, bool x_bf16, const GemvArgs& a, const TmaConfig& c, cudaStream_t s);
 
 // Host launchers (gemv.cu / quantize.cu).
 cudaError_t launch_gemv(int epi, bool x_bf16, const GemvArgs& a, GemvConfig cfg, cudaStream_t s);

@@ -32,19 +32,19 @@ struct GemvDispatch {
 #define NF4_GEMV_DEFINE_DISPATCH(E)                                                               \
   template <>                                                                                     \
   const void* GemvDispatch<E>::ptr(int nch, int rb, bool big, bool xb) {                          \
-    NF4_PTR_CASE(E, 1, 2, false, 256) NF4_PTR_CASE(E, 1, 4, false, 256)                           \
-    NF4_PTR_CASE(E, 1, 8, false, 256) NF4_PTR_CASE(E, 2, 2, false, 256)                           \
-    NF4_PTR_CASE(E, 2, 4, false, 256) NF4_PTR_CASE(E, 1, 2, true, 1024)                           \
-    NF4_PTR_CASE(E, 2, 2, true, 1024)                                                             \
+    NF4_PTR_CASE(E, 1, 2, false, false) NF4_PTR_CASE(E, 1, 4, false, false)                           \
+    NF4_PTR_CASE(E, 1, 8, false, false) NF4_PTR_CASE(E, 2, 2, false, false)                           \
+    NF4_PTR_CASE(E, 2, 4, false, false) NF4_PTR_CASE(E, 1, 2, true, true)                           \
+    NF4_PTR_CASE(E, 2, 2, true, true)                                                             \
     return nullptr;                                                                               \
   }                                                                                               \
   template <>                                                                                     \
   cudaError_t GemvDispatch<E>::launch(int nch, int rb, bool big, bool xb, const GemvArgs& a,      \
                                       const GemvConfig& c, cudaStream_t s) {                      \
-    NF4_LAUNCH_CASE(E, 1, 2, false, 256) NF4_LAUNCH_CASE(E, 1, 4, false, 256)                     \
-    NF4_LAUNCH_CASE(E, 1, 8, false, 256) NF4_LAUNCH_CASE(E, 2, 2, false, 256)                     \
-    NF4_LAUNCH_CASE(E, 2, 4, false, 256) NF4_LAUNCH_CASE(E, 1, 2, true, 1024)                     \
-    NF4_LAUNCH_CASE(E, 2, 2, true, 1024)                                                          \
+    NF4_LAUNCH_CASE(E, 1, 2, false, false) NF4_LAUNCH_CASE(E, 1, 4, false, false)                     \
+    NF4_LAUNCH_CASE(E, 1, 8, false, false) NF4_LAUNCH_CASE(E, 2, 2, false, false)                     \
+    NF4_LAUNCH_CASE(E, 2, 4, false, false) NF4_LAUNCH_CASE(E, 1, 2, true, true)                     \
+    NF4_LAUNCH_CASE(E, 2, 2, true, true)                                                          \
     return cudaErrorInvalidValue;                                                                 \
   }
 

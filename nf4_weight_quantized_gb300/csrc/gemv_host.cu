@@ -13,6 +13,7 @@
 #include <tuple>
 
 #include "gemv_dispatch.cuh"
+#include "gemv_tma_dispatch.cuh"
 
 namespace nf4k {
 
@@ -53,6 +54,16 @@ struct Key {
 
 std::mutex g_mu;
 std::map<Key, GemvConfig> g_cache;
+std::map<Key, TmaConfig> g_tma_cache;
+
+const void* tma_ptr(int epi, int nch, int rb, bool xb, int lut) {
+  switch (epi) {
+    case EPI_PLAIN: return GemvTmaDispatch<EPI_PLAIN>::ptr(nch, rb, xb, lut);
+    case EPI_RESID: return GemvTmaDispatch<EPI_RESID>::ptr(nch, rb, xb, lut);
+    case EPI_SWIGLU: return GemvTmaDispatch<EPI_SWIGLU>::ptr(nch, rb, xb, lut);
+    default: return GemvTmaDispatch<EPI_ARGMAX>::ptr(nch, rb, xb, lut);
+  }
+}
 
 }  // namespace
 
@@ -121,6 +132,99 @@ GemvConfig choose_gemv_config(int epi, int64_t M, int64_t K, int device) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_cache[Key{epi, device, M, K}] = c;
   return c;
+}
+
+// Bulk-copy kernel: x-stationary row groups as in the register kernel, plus a
+// producer warp and a ring of S stages of SR rows each, one block per SM.
+TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_tma_cache.find(Key{epi, device, M, K});
+    if (it != g_tma_cache.end()) return it->second;
+  }
+  TmaConfig c{};
+  c.ok = false;
+  const bool two = (epi == EPI_SWIGLU);
+  const int nv = two ? 2 : 1;
+  const int H = (int)(K / 32);
+  if (K % 256 != 0) return c;  // scale rows must be whole 16-byte units for the bulk copies
+  if (H <= 32) {
+    c.nch = 1;
+    c.G = 32;
+  } else if (H <= 64) {
+    c.nch = 1;
+    c.G = 64;
+  } else if (32 * ((H + 31) / 32) <= 992) {
+    c.nch = 1;
+    c.G = 32 * ((H + 31) / 32);
+  } else {
+    c.nch = 2;
+    c.G = 32 * ((H + 63) / 64);
+  }
+  c.rb = env_int("NF4_TMA_RB", 2);
+  c.lut = env_int("NF4_LUT", LUT_F32);
+  if (!gemv_tma_variant_exists(c.nch, c.rb) || c.lut < 0 || c.lut > 2) return c;
+  const void* fn = tma_ptr(epi, c.nch, c.rb, true, c.lut);
+  cudaFuncAttributes attr{};
+  if (cudaFuncGetAttributes(&attr, fn) != cudaSuccess) {
+    cudaGetLastError();
+    return c;
+  }
+  const int target = env_int("NF4_TMA_THREADS", 512);
+  int gpc = (target + c.G / 2) / c.G;
+  gpc = gpc < 1 ? 1 : (gpc > 15 ? 15 : gpc);
+  while (gpc > 1 && gpc * c.G + 32 > attr.maxThreadsPerBlock) --gpc;
+  if (gpc * c.G + 32 > attr.maxThreadsPerBlock) return c;
+  c.gpc = gpc;
+  c.threads = gpc * c.G + 32;
+  c.SR = gpc * c.rb;
+  const int row_bytes = (int)(K / 2), srow_bytes = (int)(K / 16);
+  c.codes_bytes = c.SR * row_bytes;
+  c.scales_bytes = c.SR * srow_bytes;
+  c.stage_bytes = nv * (c.codes_bytes + c.scales_bytes);
+  const int red_bytes = gpc * 2 * nv * c.rb * (c.G / 32) * (int)sizeof(float);
+  int optin = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  const int avail = optin - (int)attr.sharedSizeBytes - LUT_BYTES - red_bytes - 8 * 2 * 8 - 256;
+  int S = avail / c.stage_bytes;
+  S = S > env_int("NF4_TMA_STAGES", 6) ? env_int("NF4_TMA_STAGES", 6) : S;
+  if (S < 2) return c;
+  c.S = S;
+  c.bar_off = LUT_BYTES + S * c.stage_bytes;
+  c.red_off = c.bar_off + 16 * S;
+  c.smem = c.red_off + red_bytes;
+  for (int xb = 0; xb < 2; ++xb)
+    cudaFuncSetAttribute(tma_ptr(epi, c.nch, c.rb, xb != 0, c.lut), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         c.smem);
+  int sms = 0, bps = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, c.threads, c.smem);
+  if (bps < 1) {
+    cudaGetLastError();
+    return c;
+  }
+  const int64_t want = (M + c.SR - 1) / c.SR;
+  const int64_t have = (int64_t)sms * bps;
+  c.blocks = (int)(want < have ? want : have);
+  c.ok = true;
+  cudaGetLastError();
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_tma_cache[Key{epi, device, M, K}] = c;
+  return c;
+}
+
+cudaError_t launch_gemv_tma(int epi, bool xb, const GemvArgs& a, const TmaConfig& c, cudaStream_t s) {
+  TmaPlan p{c.SR, c.S, c.stage_bytes, c.codes_bytes, c.scales_bytes, c.bar_off, c.red_off};
+  switch (epi) {
+    case EPI_PLAIN:
+      return GemvTmaDispatch<EPI_PLAIN>::launch(c.nch, c.rb, xb, c.lut, a, p, c.blocks, c.threads, c.smem, s);
+    case EPI_RESID:
+      return GemvTmaDispatch<EPI_RESID>::launch(c.nch, c.rb, xb, c.lut, a, p, c.blocks, c.threads, c.smem, s);
+    case EPI_SWIGLU:
+      return GemvTmaDispatch<EPI_SWIGLU>::launch(c.nch, c.rb, xb, c.lut, a, p, c.blocks, c.threads, c.smem, s);
+    default:
+      return GemvTmaDispatch<EPI_ARGMAX>::launch(c.nch, c.rb, xb, c.lut, a, p, c.blocks, c.threads, c.smem, s);
+  }
 }
 
 cudaError_t launch_gemv(int epi, bool xb, const GemvArgs& a, GemvConfig cfg, cudaStream_t s) {

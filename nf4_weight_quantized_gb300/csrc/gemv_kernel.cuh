@@ -96,11 +96,8 @@ struct Batch {
   float s[NV][RB][NCH];
 };
 
-// MAXT bounds the block size the instantiation is compiled for: 256 leaves the
-// register allocation free (up to 255 per thread); 1024 caps it at 64 so that
-// one row group can span a whole block for very long rows (K > ~20k).
-template <int NCH, int RB, int EPI, bool XBF16, int MAXT>
-__global__ void __launch_bounds__(MAXT) gemv_kernel(const __grid_constant__ GemvArgs a) {
+template <int NCH, int RB, int EPI, bool XBF16>
+__device__ __forceinline__ void gemv_body(const GemvArgs& a) {
   constexpr int NV = (EPI == EPI_SWIGLU) ? 2 : 1;  // matrices per row
   constexpr int P = Log2<RB>::value;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -301,16 +298,33 @@ __global__ void __launch_bounds__(MAXT) gemv_kernel(const __grid_constant__ Gemv
   }
 }
 
-// Launch one instantiation with the given configuration.
-template <int NCH, int RB, int EPI, bool XBF16, int MAXT>
-cudaError_t launch_gemv_instance(const GemvArgs& a, const GemvConfig& cfg, cudaStream_t s) {
-  gemv_kernel<NCH, RB, EPI, XBF16, MAXT><<<cfg.blocks, cfg.G * cfg.gpc, cfg.smem, s>>>(a);
-  return cudaGetLastError();
+// The register allocation is left free (up to 255 per thread) ...
+template <int NCH, int RB, int EPI, bool XBF16>
+__global__ void gemv_kernel(const __grid_constant__ GemvArgs a) {
+  gemv_body<NCH, RB, EPI, XBF16>(a);
 }
 
-template <int NCH, int RB, int EPI, bool XBF16, int MAXT>
+// ... or capped at 64 so that one row group can span a 1024-thread block for
+// very long rows (K above ~20k).
+template <int NCH, int RB, int EPI, bool XBF16>
+__global__ void __launch_bounds__(1024) gemv_kernel_big(const __grid_constant__ GemvArgs a) {
+  gemv_body<NCH, RB, EPI, XBF16>(a);
+}
+
+template <int NCH, int RB, int EPI, bool XBF16, bool BIG>
 const void* gemv_instance_ptr() {
-  return reinterpret_cast<const void*>(&gemv_kernel<NCH, RB, EPI, XBF16, MAXT>);
+  return BIG ? reinterpret_cast<const void*>(&gemv_kernel_big<NCH, RB, EPI, XBF16>)
+             : reinterpret_cast<const void*>(&gemv_kernel<NCH, RB, EPI, XBF16>);
+}
+
+// Launch one instantiation with the given configuration.
+template <int NCH, int RB, int EPI, bool XBF16, bool BIG>
+cudaError_t launch_gemv_instance(const GemvArgs& a, const GemvConfig& cfg, cudaStream_t s) {
+  if (BIG)
+    gemv_kernel_big<NCH, RB, EPI, XBF16><<<cfg.blocks, cfg.G * cfg.gpc, cfg.smem, s>>>(a);
+  else
+    gemv_kernel<NCH, RB, EPI, XBF16><<<cfg.blocks, cfg.G * cfg.gpc, cfg.smem, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace nf4k

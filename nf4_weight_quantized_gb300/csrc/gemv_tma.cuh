@@ -1,0 +1,347 @@
+// gemv_tma.cuh -- N=1 NF4 GEMV with bulk-copy (TMA engine) weight streaming.
+//
+// Same arithmetic and epilogues as gemv_kernel.cuh (source: "Decode V2 --
+// resident executor", section 6 "Linear primitive"), different data movement:
+//  * each block owns a contiguous range of rows, whose codes and scales are
+//    contiguous in memory; one producer thread streams them into a ring of S
+//    shared-memory stages with 1-D cp.async.bulk copies completing on mbarriers
+//    ("full"), marked evict-first in L2 since every weight is read once;
+//  * consumer warps are x-stationary as before (thread t of a row group always
+//    owns chunks t + G*j of a row, its x slice lives in registers) and read the
+//    codes of each staged row from shared memory (conflict-free 16-byte loads),
+//    then release the stage ("empty") for the producer to refill.
+// Bytes in flight per SM are set by the ring (tens of KB), not by how many
+// registers the consumers can spare, which is what bounded the register-
+// prefetch kernel.  Every barrier wait is bounded (mbar_wait_bounded).
+//
+// Dequantization modes (LUTM):
+//  LUT_F32  pair table of exact fp32 levels: per code byte one PRMT, one
+//           conflict-free LDS.64, two FFMAs (or one packed FFMA2).
+//  LUT_F16  pair table of fp16-rounded levels (relative error <= 2^-12 per
+//           level): one LDS.32 per code byte halves the shared-memory traffic,
+//           two conversions to fp32, then fp32 FMAs.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gemv_kernel.cuh"
+
+namespace nf4k {
+
+enum LutMode : int { LUT_F32 = 0, LUT_F16 = 1, LUT_F32X2 = 2 };
+
+// Shared-memory plan of one launch (host-computed).
+struct TmaPlan {
+  int SR;          // rows per stage (= gpc * RB)
+  int S;           // stages
+  int stage_bytes; // bytes of one stage (all matrices: codes then scales)
+  int codes_bytes; // SR * K/2, one matrix
+  int scales_bytes;// SR * K/64 * 4, one matrix
+  int bar_off;     // offset of the 2*S mbarriers
+  int red_off;     // offset of the reduction buffers
+};
+
+template <int LUTM>
+__device__ __forceinline__ float chunk_dot_t(const uint4 c, const float (&xv)[32], uint32_t laneoff,
+                                             const uint8_t* lut) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  if (LUTM == LUT_F16) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t off = __byte_perm(w[q], laneoff, 0x5504u | (j << 4));
+        const __half2 h = *reinterpret_cast<const __half2*>(lut + off);
+        const float2 v = __half22float2(h);
+        acc[j] = fmaf(v.x, xv[8 * q + 2 * j], acc[j]);
+        acc[j] = fmaf(v.y, xv[8 * q + 2 * j + 1], acc[j]);
+      }
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  } else if (LUTM == LUT_F32X2) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t off = __byte_perm(w[q], laneoff, 0x5504u | (j << 4));
+        const float2 v = *reinterpret_cast<const float2*>(lut + off);
+        ffma2(acc[2 * j], acc[2 * j + 1], v.x, v.y, xv[8 * q + 2 * j], xv[8 * q + 2 * j + 1]);
+      }
+    }
+    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  } else {
+    return chunk_dot(c, xv, laneoff, lut);
+  }
+}
+
+template <int NCH, int RB, int EPI, bool XBF16, int LUTM>
+__global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid_constant__ TmaPlan P) {
+  constexpr int NV = (EPI == EPI_SWIGLU) ? 2 : 1;
+  constexpr int PL = Log2<RB>::value;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ float cbs[16];
+  __shared__ unsigned long long warp_keys[32];
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int G = a.G;
+  const int NC = G * a.gpc;  // consumer threads; the last warp produces
+  const bool is_producer = tid >= NC;
+  const int group = is_producer ? 0 : tid / G;
+  const int t = tid - group * G;
+  const int wig = t >> 5;
+  const int WPG = G >> 5;
+  const int H = a.K >> 5;
+  const int64_t R0 = (int64_t)blockIdx.x * a.M / gridDim.x;
+  const int64_t R1 = (int64_t)(blockIdx.x + 1) * a.M / gridDim.x;
+  const int n_it = (int)((R1 - R0 + P.SR - 1) / P.SR);
+  const int row_bytes = a.K >> 1;
+  const int nblk = a.K >> 6;
+
+  uint8_t* stages = smem + LUT_BYTES;
+  const uint32_t bar0 = smem_addr(smem + P.bar_off);  // full[s] at bar0 + 8s, empty[s] at bar0 + 8(S+s)
+  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(P.S + s); };
+
+  if (tid == NC) {
+    for (int s = 0; s < P.S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), (uint32_t)(NC >> 5));
+    }
+    mbar_init_fence();
+    s_abort = 0;
+  }
+  if (tid < 16) cbs[tid] = a.cb.v[tid];
+  __syncthreads();
+
+  // producer: issue the first S stages before anything else
+  uint64_t policy = 0;
+  const uint8_t* mcodes[NV];
+  const float* mscales[NV];
+  mcodes[0] = a.codes;
+  mscales[0] = a.scales;
+  if (NV == 2) {
+    mcodes[NV - 1] = a.codes2;
+    mscales[NV - 1] = a.scales2;
+  }
+  auto issue = [&](int it) {
+    const int s = it % P.S;
+    const int64_t rb = R0 + (int64_t)it * P.SR;
+    const int rows = (int)((R1 - rb) < P.SR ? (R1 - rb) : P.SR);
+    const uint32_t cb = (uint32_t)rows * (uint32_t)row_bytes;
+    const uint32_t sb = (uint32_t)rows * (uint32_t)nblk * 4u;
+    mbar_arrive_expect_tx(full_bar(s), NV * (cb + sb));
+    uint8_t* st = stages + (size_t)s * P.stage_bytes;
+#pragma unroll
+    for (int n = 0; n < NV; ++n) {
+      bulk_g2s(smem_addr(st + n * P.codes_bytes), mcodes[n] + rb * row_bytes, cb, full_bar(s), policy);
+      bulk_g2s(smem_addr(st + NV * P.codes_bytes + n * P.scales_bytes), mscales[n] + rb * nblk, sb,
+               full_bar(s), policy);
+    }
+  };
+  int issued = 0;
+  if (is_producer && lane == 0) {
+    policy = policy_evict_first();
+    for (; issued < n_it && issued < P.S; ++issued) issue(issued);
+  }
+
+  // consumers: x slice to registers
+  int cidx[NCH];
+  bool cval[NCH];
+  float xv[NCH][32];
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    cidx[j] = t + G * j;
+    cval[j] = !is_producer && cidx[j] < H;
+    if (cval[j]) {
+      if (XBF16) {
+        const uint8_t* xp = reinterpret_cast<const uint8_t*>(a.x) + (int64_t)cidx[j] * 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 u = ld_nc_v4(xp + 16 * q);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            xv[j][8 * q + 2 * e] = bf16lo_to_f32(w[e]);
+            xv[j][8 * q + 2 * e + 1] = bf16hi_to_f32(w[e]);
+          }
+        }
+      } else {
+        const uint8_t* xp = reinterpret_cast<const uint8_t*>(a.x) + (int64_t)cidx[j] * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 u = ld_nc_v4(xp + 16 * q);
+          xv[j][4 * q + 0] = __uint_as_float(u.x);
+          xv[j][4 * q + 1] = __uint_as_float(u.y);
+          xv[j][4 * q + 2] = __uint_as_float(u.z);
+          xv[j][4 * q + 3] = __uint_as_float(u.w);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) xv[j][e] = 0.f;
+    }
+  }
+
+  // pair table: byte b, lane l -> (cb[b & 15], cb[b >> 4]) at b * 256 + l * (8 or 4)
+  if (LUTM == LUT_F16) {
+    for (int i = tid; i < 256 * 32; i += blockDim.x) {
+      const int b = i >> 5, l = i & 31;
+      *reinterpret_cast<__half2*>(smem + b * 256 + l * 4) = __floats2half2_rn(cbs[b & 15], cbs[b >> 4]);
+    }
+  } else {
+    for (int i = tid; i < 256 * 32; i += blockDim.x) {
+      const int b = i >> 5;
+      reinterpret_cast<float2*>(smem)[i] = make_float2(cbs[b & 15], cbs[b >> 4]);
+    }
+  }
+  __syncthreads();
+
+  volatile int* abort = &s_abort;
+  unsigned long long best = 0ull;
+
+  if (is_producer) {
+    if (lane == 0) {
+      for (; issued < n_it; ++issued) {
+        const int s = issued % P.S;
+        // the consumers released this stage's previous use (iteration issued - S)
+        if (!mbar_wait_bounded(empty_bar(s), (uint32_t)(((issued / P.S) - 1) & 1), abort)) break;
+        issue(issued);
+      }
+      if (*abort) {
+        // drain: wait (bounded, ignoring the abort flag) for every copy that
+        // may still be in flight, so none lands after the block has exited
+        for (int it = (issued > P.S ? issued - P.S : 0); it < issued; ++it)
+          for (uint32_t i = 0; i < kWaitPolls; ++i)
+            if (mbar_try_wait(full_bar(it % P.S), (uint32_t)((it / P.S) & 1))) break;
+      }
+    }
+  } else {
+    const uint8_t* lut = smem;
+    const uint32_t laneoff = (uint32_t)lane * (LUTM == LUT_F16 ? 4u : 8u);
+    float* red = reinterpret_cast<float*>(smem + P.red_off) + group * (2 * NV * RB * WPG);
+    int buf = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % P.S;
+      mbar_wait_bounded(full_bar(s), (uint32_t)((it / P.S) & 1), abort);
+      const int64_t rb = R0 + (int64_t)it * P.SR;
+      const int rows = (int)((R1 - rb) < P.SR ? (R1 - rb) : P.SR);
+      const uint8_t* st = stages + (size_t)s * P.stage_bytes;
+      float acc[NV][RB];
+#pragma unroll
+      for (int n = 0; n < NV; ++n) {
+        const uint8_t* sc = st + n * P.codes_bytes;
+        const float* ss = reinterpret_cast<const float*>(st + NV * P.codes_bytes + n * P.scales_bytes);
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+          const int lr = group * RB + i;
+          float r = 0.f;
+          if (lr < rows) {
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+              if (cval[j]) {
+                const uint4 c = lds128(sc + lr * row_bytes + cidx[j] * 16);
+                const float scale = ss[lr * nblk + (cidx[j] >> 1)];
+                r = fmaf(chunk_dot_t<LUTM>(c, xv[j], laneoff, lut), scale, r);
+              }
+            }
+          }
+          acc[n][i] = r;
+        }
+      }
+      // the stage's shared memory is no longer read by this warp
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(s));
+
+      float v[NV];
+#pragma unroll
+      for (int n = 0; n < NV; ++n) v[n] = transpose_reduce<RB>(acc[n], lane);
+      const int rs = (PL == 0) ? 0 : (lane >> (5 - PL));
+      const bool rep = (lane & ((32 >> PL) - 1)) == 0;
+      int lr = -1;
+      if (WPG == 1) {
+        if (rep) lr = group * RB + rs;
+      } else {
+        float* rbuf = red + buf * (NV * RB * WPG);
+        if (rep) {
+#pragma unroll
+          for (int n = 0; n < NV; ++n) rbuf[(n * RB + rs) * WPG + wig] = v[n];
+        }
+        named_bar_sync(1 + group, G);
+        if (t < RB) {
+          lr = group * RB + t;
+#pragma unroll
+          for (int n = 0; n < NV; ++n) {
+            float sum = 0.f;
+            for (int w = 0; w < WPG; ++w) sum += rbuf[(n * RB + t) * WPG + w];
+            v[n] = sum;
+          }
+        }
+        buf ^= 1;
+      }
+      if (lr >= 0 && lr < rows && !*abort) {
+        const int64_t row = rb + lr;
+        if (EPI == EPI_PLAIN) {
+          a.y[row] = v[0];
+        } else if (EPI == EPI_RESID) {
+          a.y[row] = v[0] + a.resid[row];
+        } else if (EPI == EPI_SWIGLU) {
+          const float g = v[0];
+          const float u = v[NV - 1];
+          const float silu = g / (1.0f + expf(-g));
+          a.out_bf16[row] = __bfloat16_as_ushort(__float2bfloat16_rn(silu * u));
+        } else {
+          a.y[row] = v[0];
+          const unsigned long long k = argmax_key(v[0], row);
+          best = k > best ? k : best;
+        }
+      }
+    }
+  }
+
+  if (EPI == EPI_ARGMAX) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+      best = o > best ? o : best;
+    }
+    if (lane == 0) warp_keys[tid >> 5] = best;
+    __syncthreads();
+    if (tid < 32) {
+      unsigned long long k = (tid < (int)(blockDim.x >> 5)) ? warp_keys[tid] : 0ull;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, k, off);
+        k = o > k ? o : k;
+      }
+      if (tid == 0) {
+        if (k) atomicMax(&a.ws[0], k);
+        __threadfence();
+        const unsigned int prev = atomicAdd(reinterpret_cast<unsigned int*>(&a.ws[1]), 1u);
+        if (prev == gridDim.x - 1) {
+          const unsigned long long fin = atomicExch(&a.ws[0], 0ull);
+          *a.index = (int64_t)(0xFFFFFFFFu - (uint32_t)(fin & 0xFFFFFFFFull));
+          atomicExch(reinterpret_cast<unsigned int*>(&a.ws[1]), 0u);
+        }
+      }
+    }
+  }
+}
+
+template <int NCH, int RB, int EPI, bool XBF16, int LUTM>
+const void* gemv_tma_ptr() {
+  return reinterpret_cast<const void*>(&gemv_tma_kernel<NCH, RB, EPI, XBF16, LUTM>);
+}
+
+template <int NCH, int RB, int EPI, bool XBF16, int LUTM>
+cudaError_t launch_gemv_tma_instance(const GemvArgs& a, const TmaPlan& p, int blocks, int threads, int smem,
+                                     cudaStream_t s) {
+  gemv_tma_kernel<NCH, RB, EPI, XBF16, LUTM><<<blocks, threads, smem, s>>>(a, p);
+  return cudaGetLastError();
+}
+
+}  // namespace nf4k

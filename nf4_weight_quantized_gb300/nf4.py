@@ -24,7 +24,8 @@ NF4_BF16 = 1
 MAX_K = 65536
 MAX_CHUNK_N = 32
 
-_STATUS = {0: "NF4_OK", -1: "NF4_EINVAL", -2: "NF4_EALIGN", -3: "NF4_ENULL", -4: "NF4_ECUDA", -5: "NF4_EARCH"}
+_STATUS = {0: "NF4_OK", -1: "NF4_EINVAL", -2: "NF4_EALIGN", -3: "NF4_ENULL", -4: "NF4_ECUDA", -5: "NF4_EARCH",
+           -6: "NF4_ETIMEOUT"}
 
 
 class NF4Error(RuntimeError):
@@ -67,13 +68,16 @@ def _load():
     lib.nf4_last_error.restype = ctypes.c_char_p
     lib.nf4_describe_config.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
     lib.nf4_describe_config.restype = ctypes.c_char_p
+    lib.nf4_check_device_errors.argtypes = []
+    lib.nf4_check_device_errors.restype = ctypes.c_int
     return lib
 
 
 lib = _load()
 
 EXPORTS = ("nf4_gemv", "nf4_gemv_residual", "nf4_gemv_swiglu", "nf4_gemv_argmax", "nf4_gemm_chunk",
-           "nf4_workspace_bytes", "nf4_quantize", "nf4_codebook", "nf4_last_error", "nf4_describe_config")
+           "nf4_workspace_bytes", "nf4_quantize", "nf4_codebook", "nf4_last_error", "nf4_describe_config",
+           "nf4_check_device_errors")
 
 
 def _check(status: int):
@@ -220,6 +224,11 @@ def nf4_codebook() -> list[float]:
 
 def nf4_describe_config(M: int, K: int, N: int = 1) -> str:
     return lib.nf4_describe_config(M, K, N).decode()
+
+
+def nf4_check_device_errors() -> None:
+    """Synchronize and raise NF4Error(NF4_ETIMEOUT) if a kernel's bounded wait ran out."""
+    _check(lib.nf4_check_device_errors())
 
 
 def nf4_last_error() -> str:

@@ -88,6 +88,26 @@ def test_gemv_shapes(nf4, M, K, xd):
     assert np.all(yh[M:] == 12345.0), "wrote past the output"
 
 
+@pytest.mark.parametrize("M,K", [(300, 2048), (2049, 11008), (77, 5120)])
+def test_register_kernel_path(nf4, M, K):
+    # scales that are 4- but not 16-byte aligned take the register-prefetch
+    # kernel instead of the bulk-copy one; both must agree with the oracle
+    seed = 150 + M
+    codes, scales = H.quantized(seed, 0, M, K)
+    x = H.make_x(seed, K, "bf16")
+    y_ref, S = oracle.gemv(codes, scales, x)
+    W = H.weight_tensors(codes, scales)
+    sc = torch.empty(scales.size + 4, dtype=torch.float32, device="cuda")
+    sc[1:1 + scales.size] = W.scales.reshape(-1)
+    W2 = nf4.NF4Weight(W.codes, sc[1:1 + scales.size].view(M, K // 64))
+    assert W2.scales.data_ptr() % 16 != 0
+    y = nf4.nf4_gemv(W2, H.x_tensor(x)).cpu().numpy()
+    H.assert_within(y, y_ref, S, what=f"register kernel {M}x{K}")
+    y_tma = nf4.nf4_gemv(W, H.x_tensor(x)).cpu().numpy()
+    H.assert_within(y_tma, y_ref, S, what=f"bulk-copy kernel {M}x{K}")
+    nf4.nf4_check_device_errors()
+
+
 def test_gemv_tiny_workload(nf4):
     w = synth.WORKLOADS["tiny"]
     d = synth.workload_inputs(w)
