@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -189,19 +190,40 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
     if (tc.ok) {
       a.G = tc.G;
       a.gpc = tc.gpc;
-      return launched(nf4k::launch_gemv_tma(epi, xt == NF4_BF16, a, tc, reinterpret_cast<cudaStream_t>(stream)),
-                      what);
+      const cudaError_t e = nf4k::launch_gemv_tma(epi, xt == NF4_BF16, a, tc, reinterpret_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess)
+        return fail(NF4_ECUDA, "%s: launch failed (bulk-copy kernel, %d blocks x %d threads, %d B shared): %s", what,
+                    tc.blocks, tc.threads, tc.smem, cudaGetErrorString(e));
+      return NF4_OK;
     }
   }
   const nf4k::GemvConfig cfg = nf4k::choose_gemv_config(epi, W->M, W->K, dev);
   a.G = cfg.G;
   a.gpc = cfg.gpc;
-  return launched(nf4k::launch_gemv(epi, xt == NF4_BF16, a, cfg, reinterpret_cast<cudaStream_t>(stream)), what);
+  const cudaError_t e = nf4k::launch_gemv(epi, xt == NF4_BF16, a, cfg, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(NF4_ECUDA, "%s: launch failed (register kernel nch=%d rb=%d%s, %d blocks x %d threads, %d B shared): %s",
+                what, cfg.nch, cfg.rb, cfg.big ? " capped" : "", cfg.blocks, cfg.G * cfg.gpc, cfg.smem,
+                cudaGetErrorString(e));
+  return NF4_OK;
 }
 
 }  // namespace
 
 namespace nf4k {
+cudaError_t ensure_smem_limit(const void* fn, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;  // (function, device) -> bytes set
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(mu);
+  int& have = done[std::make_pair(fn, dev)];
+  if (have >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
 void register_device_error_reader(DeviceErrorReader f) {
   std::lock_guard<std::mutex> lk(readers_mu());
   readers().push_back(f);
@@ -285,8 +307,9 @@ nf4_status nf4_gemm_chunk(const nf4_weight* W, const uint16_t* X, int N, float* 
 
 size_t nf4_workspace_bytes(int64_t M, int64_t K, int N) {
   if (M < 1 || K < 64 || K % 64 || N < 1 || N > NF4_MAX_CHUNK_N) return 0;
-  if (N == 1) return 16;  // argmax: 64-bit key + block ticket
-  return nf4k::chunk_workspace_bytes(M, K, N);
+  // argmax (N = 1): 64-bit key + block ticket; chunk: split-K partials + tickets
+  const size_t chunk = nf4k::chunk_workspace_bytes(M, K, N);
+  return N == 1 ? (chunk > 16 ? chunk : 16) : chunk;
 }
 
 nf4_status nf4_quantize(const float* W, int64_t M, int64_t K, uint8_t* codes, float* scales, nf4_stream stream) {

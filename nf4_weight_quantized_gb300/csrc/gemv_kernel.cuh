@@ -320,6 +320,8 @@ const void* gemv_instance_ptr() {
 // Launch one instantiation with the given configuration.
 template <int NCH, int RB, int EPI, bool XBF16, bool BIG>
 cudaError_t launch_gemv_instance(const GemvArgs& a, const GemvConfig& cfg, cudaStream_t s) {
+  const cudaError_t e = ensure_smem_limit(gemv_instance_ptr<NCH, RB, EPI, XBF16, BIG>(), cfg.smem);
+  if (e != cudaSuccess) return e;
   if (BIG)
     gemv_kernel_big<NCH, RB, EPI, XBF16><<<cfg.blocks, cfg.G * cfg.gpc, cfg.smem, s>>>(a);
   else
