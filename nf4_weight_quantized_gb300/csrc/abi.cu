@@ -149,7 +149,8 @@ nf4_status check_out(const void* p, size_t align, const char* name, const char* 
 }
 
 nf4_status launched(cudaError_t e, const char* what) {
-  if (e != cudaSuccess) return fail(NF4_ECUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  const std::string note = nf4k::take_launch_note();
+  if (e != cudaSuccess) return fail(NF4_ECUDA, "%s: launch failed: %s%s", what, cudaGetErrorString(e), note.c_str());
   return NF4_OK;
 }
 
@@ -192,8 +193,8 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
       a.gpc = tc.gpc;
       const cudaError_t e = nf4k::launch_gemv_tma(epi, xt == NF4_BF16, a, tc, reinterpret_cast<cudaStream_t>(stream));
       if (e != cudaSuccess)
-        return fail(NF4_ECUDA, "%s: launch failed (bulk-copy kernel, %d blocks x %d threads, %d B shared): %s", what,
-                    tc.blocks, tc.threads, tc.smem, cudaGetErrorString(e));
+        return fail(NF4_ECUDA, "%s: launch failed (bulk-copy kernel, %d blocks x %d threads, %d B shared): %s%s",
+                    what, tc.blocks, tc.threads, tc.smem, cudaGetErrorString(e), nf4k::take_launch_note().c_str());
       return NF4_OK;
     }
   }
@@ -202,9 +203,10 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
   a.gpc = cfg.gpc;
   const cudaError_t e = nf4k::launch_gemv(epi, xt == NF4_BF16, a, cfg, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
-    return fail(NF4_ECUDA, "%s: launch failed (register kernel nch=%d rb=%d%s, %d blocks x %d threads, %d B shared): %s",
-                what, cfg.nch, cfg.rb, cfg.big ? " capped" : "", cfg.blocks, cfg.G * cfg.gpc, cfg.smem,
-                cudaGetErrorString(e));
+    return fail(NF4_ECUDA,
+                "%s: launch failed (register kernel nch=%d rb=%d%s, %d blocks x %d threads, %d B shared): %s%s", what,
+                cfg.nch, cfg.rb, cfg.big ? " capped" : "", cfg.blocks, cfg.G * cfg.gpc, cfg.smem,
+                cudaGetErrorString(e), nf4k::take_launch_note().c_str());
   return NF4_OK;
 }
 
@@ -222,6 +224,37 @@ cudaError_t ensure_smem_limit(const void* fn, int bytes) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) have = bytes;
   return e;
+}
+
+thread_local std::string g_launch_note;
+
+void note_launch_failure(const void* fn, int threads, int smem, cudaError_t set_err, cudaError_t launch_err,
+                         cudaError_t retry_err) {
+  cudaFuncAttributes at{};
+  const cudaError_t ae = cudaFuncGetAttributes(&at, fn);
+  cudaGetLastError();
+  char buf[512];
+  std::snprintf(buf, sizeof buf,
+                " [first attempt: limit %s, launch %s; retry %s; requested %d threads, %d B dynamic shared; "
+                "function: %s, %d regs, %zu B static shared, max %d B dynamic, max %d threads]",
+                cudaGetErrorName(set_err), cudaGetErrorName(launch_err), cudaGetErrorName(retry_err), threads, smem,
+                cudaGetErrorName(ae), at.numRegs, at.sharedSizeBytes, at.maxDynamicSharedSizeBytes,
+                at.maxThreadsPerBlock);
+  g_launch_note = buf;
+}
+
+void note_stale_error(const void* fn, cudaError_t stale) {
+  static const bool on = [] {
+    const char* e = std::getenv("NF4_DEBUG_LAUNCH");
+    return e && *e == '1';
+  }();
+  if (on) std::fprintf(stderr, "nf4: stale CUDA error before launching %p: %s\n", fn, cudaGetErrorName(stale));
+}
+
+std::string take_launch_note() {
+  std::string s;
+  s.swap(g_launch_note);
+  return s;
 }
 
 void register_device_error_reader(DeviceErrorReader f) {

@@ -299,11 +299,9 @@ cudaError_t launch_chunk(const uint8_t* codes, const float* scales, int M, int K
   }
   a.S = 4;
   const int smem = LUT_BYTES + a.S * STAGE_BYTES;
-  const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(&chunk_kernel), smem);
-  if (e != cudaSuccess) return e;
   const int tiles = (M + TILE_M - 1) / TILE_M;
-  chunk_kernel<<<tiles * a.P, NTHREADS, smem, s>>>(a);
-  return cudaGetLastError();
+  return checked_launch(reinterpret_cast<const void*>(&chunk_kernel), NTHREADS, smem,
+                        [&] { chunk_kernel<<<tiles * a.P, NTHREADS, smem, s>>>(a); });
 }
 
 std::string describe_chunk(int64_t M, int64_t K, int N, int device) {

@@ -252,6 +252,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // (host; once per function and size, thread-safe).
 cudaError_t ensure_smem_limit(const void* fn, int bytes);
 
+// Launch helper used by every kernel wrapper: raises the shared-memory limit,
+// launches, and on failure records what failed (attribute or launch, the
+// function's attributes) for the caller's error message, then re-applies the
+// limit and retries the launch once.
+template <typename Launch>
+cudaError_t checked_launch(const void* fn, int threads, int smem, Launch&& launch);
+void note_launch_failure(const void* fn, int threads, int smem, cudaError_t set_err, cudaError_t launch_err,
+                         cudaError_t retry_err);
+std::string take_launch_note();
+void note_stale_error(const void* fn, cudaError_t stale);  // NF4_DEBUG_LAUNCH=1 prints it
+
+template <typename Launch>
+cudaError_t checked_launch(const void* fn, int threads, int smem, Launch&& launch) {
+  const cudaError_t stale = cudaGetLastError();  // launch errors below are this launch's own
+  if (stale != cudaSuccess) note_stale_error(fn, stale);
+  const cudaError_t set_err = ensure_smem_limit(fn, smem);
+  cudaError_t e = set_err;
+  if (e == cudaSuccess) {
+    launch();
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) return e;
+  // re-apply the limit unconditionally and retry once
+  cudaError_t retry = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (retry == cudaSuccess) {
+    launch();
+    retry = cudaGetLastError();
+  } else {
+    cudaGetLastError();
+  }
+  note_launch_failure(fn, threads, smem, set_err, e, retry);
+  return retry;
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

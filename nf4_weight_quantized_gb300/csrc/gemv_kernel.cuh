@@ -320,13 +320,12 @@ const void* gemv_instance_ptr() {
 // Launch one instantiation with the given configuration.
 template <int NCH, int RB, int EPI, bool XBF16, bool BIG>
 cudaError_t launch_gemv_instance(const GemvArgs& a, const GemvConfig& cfg, cudaStream_t s) {
-  const cudaError_t e = ensure_smem_limit(gemv_instance_ptr<NCH, RB, EPI, XBF16, BIG>(), cfg.smem);
-  if (e != cudaSuccess) return e;
-  if (BIG)
-    gemv_kernel_big<NCH, RB, EPI, XBF16><<<cfg.blocks, cfg.G * cfg.gpc, cfg.smem, s>>>(a);
-  else
-    gemv_kernel<NCH, RB, EPI, XBF16><<<cfg.blocks, cfg.G * cfg.gpc, cfg.smem, s>>>(a);
-  return cudaGetLastError();
+  return checked_launch(gemv_instance_ptr<NCH, RB, EPI, XBF16, BIG>(), cfg.G * cfg.gpc, cfg.smem, [&] {
+    if (BIG)
+      gemv_kernel_big<NCH, RB, EPI, XBF16><<<cfg.blocks, cfg.G * cfg.gpc, cfg.smem, s>>>(a);
+    else
+      gemv_kernel<NCH, RB, EPI, XBF16><<<cfg.blocks, cfg.G * cfg.gpc, cfg.smem, s>>>(a);
+  });
 }
 
 }  // namespace nf4k

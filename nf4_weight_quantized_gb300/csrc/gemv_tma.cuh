@@ -340,10 +340,9 @@ const void* gemv_tma_ptr() {
 template <int NCH, int RB, int EPI, bool XBF16, int LUTM>
 cudaError_t launch_gemv_tma_instance(const GemvArgs& a, const TmaPlan& p, int blocks, int threads, int smem,
                                      cudaStream_t s) {
-  const cudaError_t e = ensure_smem_limit(gemv_tma_ptr<NCH, RB, EPI, XBF16, LUTM>(), smem);
-  if (e != cudaSuccess) return e;
-  gemv_tma_kernel<NCH, RB, EPI, XBF16, LUTM><<<blocks, threads, smem, s>>>(a, p);
-  return cudaGetLastError();
+  return checked_launch(gemv_tma_ptr<NCH, RB, EPI, XBF16, LUTM>(), threads, smem, [&] {
+    gemv_tma_kernel<NCH, RB, EPI, XBF16, LUTM><<<blocks, threads, smem, s>>>(a, p);
+  });
 }
 
 }  // namespace nf4k
