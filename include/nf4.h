@@ -143,6 +143,27 @@ nf4_status nf4_gemv_argmax(const nf4_weight* W, const void* x, nf4_dtype xt, flo
 nf4_status nf4_gemm_chunk(const nf4_weight* W, const uint16_t* X, int N, float* Y, void* workspace,
                           nf4_stream stream);
 
+/*
+ * nf4_gemm_chunk without a caller workspace, for callers that cannot allocate
+ * device memory: a host program that owns every allocation and hands this
+ * library only its inputs and outputs, or a loop that must not call
+ * cudaMalloc (it synchronizes the device).  There is no counterpart on the
+ * source pages; the arithmetic, arguments and errors are those of
+ * nf4_gemm_chunk.
+ *   Scratch: one 8 MiB array in the library's device memory, reserved on
+ *   every GPU that loads the library until the process exits.  Shapes whose
+ *   nf4_workspace_bytes(M, K, N) exceeds 8 MiB are rejected with NF4_EINVAL
+ *   and a message; use nf4_gemm_chunk for them.  (The 13824 x 5120 weight at
+ *   N = 32 needs about 7.1 MB.)
+ *   The first call on a device looks the array's device address up, with that
+ *   device current; make it before any stream capture.  Every call on a device
+ *   shares the array: calls whose kernels may overlap on the GPU (different
+ *   streams or host threads) race and must be serialized by the caller.  Each
+ *   call clears the part of the scratch that must start at zero, then launches
+ *   on `stream`.  Nothing is allocated.
+ */
+nf4_status nf4_gemm_chunk_noalloc(const nf4_weight* W, const uint16_t* X, int N, float* Y, nf4_stream stream);
+
 /* Workspace bytes that nf4_gemv_argmax (N = 1) or nf4_gemm_chunk (N > 1) need
  * for an M x K weight; the caller allocates it once (arena). */
 size_t nf4_workspace_bytes(int64_t M, int64_t K, int N);

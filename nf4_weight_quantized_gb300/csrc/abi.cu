@@ -213,6 +213,8 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
 }  // namespace
 
 namespace nf4k {
+void set_last_error(const char* msg) { g_last_error = msg; }
+
 cudaError_t ensure_smem_limit(const void* fn, int bytes) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, int> done;  // (function, device) -> bytes set

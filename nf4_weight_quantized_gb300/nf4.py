@@ -54,6 +54,7 @@ def _load():
         "nf4_gemv_swiglu": [W, W, P, I, P, P],
         "nf4_gemv_argmax": [W, P, I, P, P, P, P],
         "nf4_gemm_chunk": [W, P, I, P, P, P],
+        "nf4_gemm_chunk_noalloc": [W, P, I, P, P],
         "nf4_quantize": [P, ctypes.c_int64, ctypes.c_int64, P, P, P],
     }
     for name, args in sig.items():
@@ -77,7 +78,7 @@ lib = _load()
 
 EXPORTS = ("nf4_gemv", "nf4_gemv_residual", "nf4_gemv_swiglu", "nf4_gemv_argmax", "nf4_gemm_chunk",
            "nf4_workspace_bytes", "nf4_quantize", "nf4_codebook", "nf4_last_error", "nf4_describe_config",
-           "nf4_check_device_errors")
+           "nf4_check_device_errors", "nf4_gemm_chunk_noalloc")
 
 
 def _check(status: int):
@@ -213,6 +214,20 @@ def nf4_gemm_chunk(W: NF4Weight, X: torch.Tensor, Y: torch.Tensor | None = None,
     _check(lib.nf4_gemm_chunk(ctypes.byref(w), _dev(X, "X", torch.bfloat16), N,
                               _dev(Y, "Y", torch.float32, N * W.M), _dev(workspace, "workspace"),
                               _stream(stream)))
+    return Y
+
+
+def nf4_gemm_chunk_noalloc(W: NF4Weight, X: torch.Tensor, Y: torch.Tensor, stream=None) -> torch.Tensor:
+    """nf4_gemm_chunk with the library's static scratch instead of a workspace.
+
+    For callers that cannot allocate device memory; Y must be passed.  Calls
+    that overlap on the GPU share the scratch and race."""
+    if X.dim() != 2 or X.shape[1] != W.K:
+        raise ValueError("X must be [N, K]")
+    N = X.shape[0]
+    w = W.struct()
+    _check(lib.nf4_gemm_chunk_noalloc(ctypes.byref(w), _dev(X, "X", torch.bfloat16), N,
+                                      _dev(Y, "Y", torch.float32, N * W.M), _stream(stream)))
     return Y
 
 

@@ -108,3 +108,13 @@ def test_no_device_is_reported_not_faked(nf4):
 
 def test_describe_config_rejects_bad_shape(nf4):
     assert "invalid shape" in nf4.nf4_describe_config(8, 100, 1)
+
+
+def test_noalloc_rejects_oversize_before_any_device_work(nf4):
+    # the scratch bound is checked on the host, before the device is touched
+    big = nf4.nf4_weight(4096, 4096, 65536, 5120)
+    st = nf4.lib.nf4_gemm_chunk_noalloc(ctypes.byref(big), ctypes.c_void_p(4096), 32, ctypes.c_void_p(4096), None)
+    assert st == -1 and "scratch" in nf4.nf4_last_error()
+    st = nf4.lib.nf4_gemm_chunk_noalloc(ctypes.byref(nf4.nf4_weight(4096, 4096, 8, 100)), ctypes.c_void_p(4096), 4,
+                                        ctypes.c_void_p(4096), None)
+    assert st == -1 and "multiple of 64" in nf4.nf4_last_error()
