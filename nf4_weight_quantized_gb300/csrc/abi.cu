@@ -228,6 +228,14 @@ cudaError_t ensure_smem_limit(const void* fn, int bytes) {
   return e;
 }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("NF4_PDL");
+    return !(e && *e == '0');
+  }();
+  return on;
+}
+
 thread_local std::string g_launch_note;
 
 void note_launch_failure(const void* fn, int threads, int smem, cudaError_t set_err, cudaError_t launch_err,
@@ -379,12 +387,23 @@ const char* nf4_describe_config(int64_t M, int64_t K, int N) {
   }
   char buf[512];
   if (N == 1) {
-    const nf4k::GemvConfig c = nf4k::choose_gemv_config(nf4k::EPI_PLAIN, M, K, dev);
-    std::snprintf(buf, sizeof buf,
-                  "gemv M=%lld K=%lld: %d thread(s) per row (%d chunk(s) of 32 weights each), %d row(s) per "
-                  "batch, %d row group(s) per block, %d blocks of %d threads, %d B shared memory%s",
-                  (long long)M, (long long)K, c.G, c.nch, c.rb, c.gpc, c.blocks, c.G * c.gpc, c.smem,
-                  c.big ? ", register-capped" : "");
+    const nf4k::TmaConfig t = use_register_kernel() ? nf4k::TmaConfig{} : nf4k::choose_tma_config(nf4k::EPI_PLAIN, M, K, dev);
+    if (t.ok) {
+      std::snprintf(buf, sizeof buf,
+                    "gemv M=%lld K=%lld (16-byte aligned scales): bulk-copy kernel, %d thread(s) per row, %d row(s) "
+                    "per group and stage, %d group(s) + 1 producer warp per block (%d threads), %d stages of %d rows "
+                    "(%d B), %d blocks, %d B shared memory, %s table, %s",
+                    (long long)M, (long long)K, t.G, t.rb, t.gpc, t.threads, t.S, t.SR, t.stage_bytes, t.blocks,
+                    t.smem, t.lut == 1 ? "fp16 pair" : "fp32 pair",
+                    nf4k::pdl_enabled() ? "programmatic dependent launch" : "plain launch");
+    } else {
+      const nf4k::GemvConfig c = nf4k::choose_gemv_config(nf4k::EPI_PLAIN, M, K, dev);
+      std::snprintf(buf, sizeof buf,
+                    "gemv M=%lld K=%lld: register kernel, %d thread(s) per row (%d chunk(s) of 32 weights each), %d "
+                    "row(s) per batch, %d row group(s) per block, %d blocks of %d threads, %d B shared memory%s",
+                    (long long)M, (long long)K, c.G, c.nch, c.rb, c.gpc, c.blocks, c.G * c.gpc, c.smem,
+                    c.big ? ", register-capped" : "");
+    }
   } else {
     std::snprintf(buf, sizeof buf, "%s", nf4k::describe_chunk(M, K, N, dev).c_str());
   }

@@ -141,6 +141,28 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel on the stream is still running.  It must not touch
+// global memory that kernel writes (or reads, for its own outputs) before
+// pdl_wait(), which returns once the previous grid has completed and its
+// writes are visible; without a programmatic dependency it returns at once.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Bring global data into L2 without touching shared memory.  Safe before
+// pdl_wait(): L2 is the point of coherence, so later reads still see writes
+// the previous kernel makes after the prefetch.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Host: programmatic dependent launch for the streaming kernels (NF4_PDL=0
+// turns it off).
+bool pdl_enabled();
+
 __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }

@@ -161,7 +161,7 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
     c.nch = 2;
     c.G = 32 * ((H + 63) / 64);
   }
-  c.rb = env_int("NF4_TMA_RB", 2);
+  c.rb = env_int("NF4_TMA_RB", 4);
   c.lut = env_int("NF4_LUT", LUT_F32);
   if (!gemv_tma_variant_exists(c.nch, c.rb) || c.lut < 0 || c.lut > 2) return c;
   const void* fn = tma_ptr(epi, c.nch, c.rb, true, c.lut);
@@ -170,7 +170,7 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
     cudaGetLastError();
     return c;
   }
-  const int target = env_int("NF4_TMA_THREADS", 512);
+  const int target = env_int("NF4_TMA_THREADS", 768);
   int gpc = (target + c.G / 2) / c.G;
   gpc = gpc < 1 ? 1 : (gpc > 15 ? 15 : gpc);
   while (gpc > 1 && gpc * c.G + 32 > attr.maxThreadsPerBlock) --gpc;

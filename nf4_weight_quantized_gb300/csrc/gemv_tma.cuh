@@ -143,11 +143,40 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
                full_bar(s), policy);
     }
   };
+  // Before the previous kernel on the stream has finished (programmatic
+  // dependent launch) only shared memory and L2 prefetches are touched.
+  pdl_launch_dependents();
   int issued = 0;
   if (is_producer && lane == 0) {
     policy = policy_evict_first();
-    for (; issued < n_it && issued < P.S; ++issued) issue(issued);
+    for (int it = 0; it < n_it && it < P.S; ++it) {
+      const int64_t rb = R0 + (int64_t)it * P.SR;
+      const int rows = (int)((R1 - rb) < P.SR ? (R1 - rb) : P.SR);
+#pragma unroll
+      for (int n = 0; n < NV; ++n) {
+        bulk_prefetch_l2(mcodes[n] + rb * row_bytes, (uint32_t)rows * (uint32_t)row_bytes);
+        bulk_prefetch_l2(mscales[n] + rb * nblk, (uint32_t)rows * (uint32_t)nblk * 4u);
+      }
+    }
   }
+
+  // pair table: byte b, lane l -> (cb[b & 15], cb[b >> 4]) at b * 256 + l * (8 or 4)
+  if (LUTM == LUT_F16) {
+    for (int i = tid; i < 256 * 32; i += blockDim.x) {
+      const int b = i >> 5, l = i & 31;
+      *reinterpret_cast<__half2*>(smem + b * 256 + l * 4) = __floats2half2_rn(cbs[b & 15], cbs[b >> 4]);
+    }
+  } else {
+    for (int i = tid; i < 256 * 32; i += blockDim.x) {
+      const int b = i >> 5;
+      reinterpret_cast<float2*>(smem)[i] = make_float2(cbs[b & 15], cbs[b >> 4]);
+    }
+  }
+
+  // everything below reads or writes global memory the previous kernel may own
+  pdl_wait();
+  if (is_producer && lane == 0)
+    for (; issued < n_it && issued < P.S; ++issued) issue(issued);
 
   // consumers: x slice to registers
   int cidx[NCH];
@@ -187,18 +216,6 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     }
   }
 
-  // pair table: byte b, lane l -> (cb[b & 15], cb[b >> 4]) at b * 256 + l * (8 or 4)
-  if (LUTM == LUT_F16) {
-    for (int i = tid; i < 256 * 32; i += blockDim.x) {
-      const int b = i >> 5, l = i & 31;
-      *reinterpret_cast<__half2*>(smem + b * 256 + l * 4) = __floats2half2_rn(cbs[b & 15], cbs[b >> 4]);
-    }
-  } else {
-    for (int i = tid; i < 256 * 32; i += blockDim.x) {
-      const int b = i >> 5;
-      reinterpret_cast<float2*>(smem)[i] = make_float2(cbs[b & 15], cbs[b >> 4]);
-    }
-  }
   __syncthreads();
 
   volatile int* abort = &s_abort;
@@ -223,6 +240,9 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
   } else {
     const uint8_t* lut = smem;
     const uint32_t laneoff = (uint32_t)lane * (LUTM == LUT_F16 ? 4u : 8u);
+    int cidx_c[NCH];
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) cidx_c[j] = cval[j] ? cidx[j] : 0;
     float* red = reinterpret_cast<float*>(smem + P.red_off) + group * (2 * NV * RB * WPG);
     int buf = 0;
     for (int it = 0; it < n_it; ++it) {
@@ -231,7 +251,11 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
       const int64_t rb = R0 + (int64_t)it * P.SR;
       const int rows = (int)((R1 - rb) < P.SR ? (R1 - rb) : P.SR);
       const uint8_t* st = stages + (size_t)s * P.stage_bytes;
-      float acc[NV][RB];
+      // Branch-free: every thread computes all RB rows of its group.  Chunks a
+      // thread does not own read chunk 0 with x = 0 and add exactly zero; rows
+      // past the end of the last stage compute garbage that is never stored.
+      uint4 c[NV][RB][NCH];
+      float scl[NV][RB][NCH];
 #pragma unroll
       for (int n = 0; n < NV; ++n) {
         const uint8_t* sc = st + n * P.codes_bytes;
@@ -239,20 +263,23 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
 #pragma unroll
         for (int i = 0; i < RB; ++i) {
           const int lr = group * RB + i;
-          float r = 0.f;
-          if (lr < rows) {
 #pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-              if (cval[j]) {
-                const uint4 c = lds128(sc + lr * row_bytes + cidx[j] * 16);
-                const float scale = ss[lr * nblk + (cidx[j] >> 1)];
-                r = fmaf(chunk_dot_t<LUTM>(c, xv[j], laneoff, lut), scale, r);
-              }
-            }
+          for (int j = 0; j < NCH; ++j) {
+            c[n][i][j] = lds128(sc + lr * row_bytes + cidx_c[j] * 16);
+            scl[n][i][j] = ss[lr * nblk + (cidx_c[j] >> 1)];
           }
-          acc[n][i] = r;
         }
       }
+      float acc[NV][RB];
+#pragma unroll
+      for (int n = 0; n < NV; ++n)
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+          float r = 0.f;
+#pragma unroll
+          for (int j = 0; j < NCH; ++j) r = fmaf(chunk_dot_t<LUTM>(c[n][i][j], xv[j], laneoff, lut), scl[n][i][j], r);
+          acc[n][i] = r;
+        }
       // the stage's shared memory is no longer read by this warp
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(s));
@@ -341,7 +368,19 @@ template <int NCH, int RB, int EPI, bool XBF16, int LUTM>
 cudaError_t launch_gemv_tma_instance(const GemvArgs& a, const TmaPlan& p, int blocks, int threads, int smem,
                                      cudaStream_t s) {
   return checked_launch(gemv_tma_ptr<NCH, RB, EPI, XBF16, LUTM>(), threads, smem, [&] {
-    gemv_tma_kernel<NCH, RB, EPI, XBF16, LUTM><<<blocks, threads, smem, s>>>(a, p);
+    // one wave of persistent blocks: the next kernel may launch early
+    // (programmatic dependent launch) and overlap its prologue with our tail
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cudaLaunchKernelEx(&cfg, gemv_tma_kernel<NCH, RB, EPI, XBF16, LUTM>, a, p);
   });
 }
 
