@@ -165,10 +165,17 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   c.lut = env_int("NF4_LUT", LUT_F32);
   if (!gemv_tma_variant_exists(c.nch, c.rb) || c.lut < 0 || c.lut > 2) return c;
   const void* fn = tma_ptr(epi, c.nch, c.rb, true, c.lut);
+  // both activation-dtype instances share the configuration: take the
+  // tighter thread limit and the larger static shared memory of the two
   cudaFuncAttributes attr{};
-  if (cudaFuncGetAttributes(&attr, fn) != cudaSuccess) {
-    cudaGetLastError();
-    return c;
+  for (int xb = 0; xb < 2; ++xb) {
+    cudaFuncAttributes ax{};
+    if (cudaFuncGetAttributes(&ax, tma_ptr(epi, c.nch, c.rb, xb != 0, c.lut)) != cudaSuccess) {
+      cudaGetLastError();
+      return c;
+    }
+    if (xb == 0 || ax.maxThreadsPerBlock < attr.maxThreadsPerBlock) attr.maxThreadsPerBlock = ax.maxThreadsPerBlock;
+    if (xb == 0 || ax.sharedSizeBytes > attr.sharedSizeBytes) attr.sharedSizeBytes = ax.sharedSizeBytes;
   }
   const int target = env_int("NF4_TMA_THREADS", 768);
   int gpc = (target + c.G / 2) / c.G;
