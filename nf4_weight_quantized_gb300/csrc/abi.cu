@@ -394,7 +394,7 @@ const char* nf4_describe_config(int64_t M, int64_t K, int N) {
                     "per group and stage, %d group(s) + 1 producer warp per block (%d threads), %d stages of %d rows "
                     "(%d B), %d blocks, %d B shared memory, %s table, %s",
                     (long long)M, (long long)K, t.G, t.rb, t.gpc, t.threads, t.S, t.SR, t.stage_bytes, t.blocks,
-                    t.smem, t.lut == 1 ? "fp16 pair" : "fp32 pair",
+                    t.smem, t.lut == 1 ? "fp16-level mixed-precision loop for bf16 x" : "fp32 pair",
                     nf4k::pdl_enabled() ? "programmatic dependent launch" : "plain launch");
     } else {
       const nf4k::GemvConfig c = nf4k::choose_gemv_config(nf4k::EPI_PLAIN, M, K, dev);

@@ -152,8 +152,9 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
     c.nch = 1;
     c.G = 32;
   } else if (H <= 64) {
-    c.nch = 1;
-    c.G = 64;
+    // one warp per row, two chunks per thread: no cross-warp reduction
+    c.nch = env_int("NF4_TMA_NCH", 2);
+    c.G = c.nch == 2 ? 32 : 64;
   } else if (32 * ((H + 31) / 32) <= 992) {
     c.nch = 1;
     c.G = 32 * ((H + 31) / 32);
@@ -161,16 +162,19 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
     c.nch = 2;
     c.G = 32 * ((H + 63) / 64);
   }
-  c.rb = env_int("NF4_TMA_RB", 4);
-  c.lut = env_int("NF4_LUT", LUT_F32);
-  if (!gemv_tma_variant_exists(c.nch, c.rb) || c.lut < 0 || c.lut > 2) return c;
-  const void* fn = tma_ptr(epi, c.nch, c.rb, true, c.lut);
+  c.rb = env_int("NF4_TMA_RB", c.nch == 1 ? 8 : 4);
+  // bf16 activations use the fp16-level mixed-precision loop unless NF4_LUT=0
+  // asks for the exact fp32 table; fp32 activations always use the fp32 table
+  c.lut = env_int("NF4_LUT", LUT_F16MIX) == LUT_F32 ? LUT_F32 : LUT_F16MIX;
+  if (!gemv_tma_variant_exists(c.nch, c.rb)) return c;
+  auto lut_for = [&](int xb) { return xb ? c.lut : (int)LUT_F32; };
+  const void* fn = tma_ptr(epi, c.nch, c.rb, true, lut_for(1));
   // both activation-dtype instances share the configuration: take the
   // tighter thread limit and the larger static shared memory of the two
   cudaFuncAttributes attr{};
   for (int xb = 0; xb < 2; ++xb) {
     cudaFuncAttributes ax{};
-    if (cudaFuncGetAttributes(&ax, tma_ptr(epi, c.nch, c.rb, xb != 0, c.lut)) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&ax, tma_ptr(epi, c.nch, c.rb, xb != 0, lut_for(xb))) != cudaSuccess) {
       cudaGetLastError();
       return c;
     }
@@ -201,7 +205,7 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   c.red_off = c.bar_off + 16 * S;
   c.smem = c.red_off + red_bytes;
   for (int xb = 0; xb < 2; ++xb)
-    cudaFuncSetAttribute(tma_ptr(epi, c.nch, c.rb, xb != 0, c.lut), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(tma_ptr(epi, c.nch, c.rb, xb != 0, lut_for(xb)), cudaFuncAttributeMaxDynamicSharedMemorySize,
                          c.smem);
   int sms = 0, bps = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
@@ -224,13 +228,13 @@ cudaError_t launch_gemv_tma(int epi, bool xb, const GemvArgs& a, const TmaConfig
   TmaPlan p{c.SR, c.S, c.stage_bytes, c.codes_bytes, c.scales_bytes, c.bar_off, c.red_off};
   switch (epi) {
     case EPI_PLAIN:
-      return GemvTmaDispatch<EPI_PLAIN>::launch(c.nch, c.rb, xb, c.lut, a, p, c.blocks, c.threads, c.smem, s);
+      return GemvTmaDispatch<EPI_PLAIN>::launch(c.nch, c.rb, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
     case EPI_RESID:
-      return GemvTmaDispatch<EPI_RESID>::launch(c.nch, c.rb, xb, c.lut, a, p, c.blocks, c.threads, c.smem, s);
+      return GemvTmaDispatch<EPI_RESID>::launch(c.nch, c.rb, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
     case EPI_SWIGLU:
-      return GemvTmaDispatch<EPI_SWIGLU>::launch(c.nch, c.rb, xb, c.lut, a, p, c.blocks, c.threads, c.smem, s);
+      return GemvTmaDispatch<EPI_SWIGLU>::launch(c.nch, c.rb, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
     default:
-      return GemvTmaDispatch<EPI_ARGMAX>::launch(c.nch, c.rb, xb, c.lut, a, p, c.blocks, c.threads, c.smem, s);
+      return GemvTmaDispatch<EPI_ARGMAX>::launch(c.nch, c.rb, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
   }
 }
 

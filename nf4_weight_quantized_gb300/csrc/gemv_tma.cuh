@@ -15,11 +15,19 @@
 // prefetch kernel.  Every barrier wait is bounded (mbar_wait_bounded).
 //
 // Dequantization modes (LUTM):
-//  LUT_F32  pair table of exact fp32 levels: per code byte one PRMT, one
-//           conflict-free LDS.64, two FFMAs (or one packed FFMA2).
-//  LUT_F16  pair table of fp16-rounded levels (relative error <= 2^-12 per
-//           level): one LDS.32 per code byte halves the shared-memory traffic,
-//           two conversions to fp32, then fp32 FMAs.
+//  LUT_F32     pair table of exact fp32 levels: per code byte one PRMT, one
+//              conflict-free LDS.64, two FFMAs.  Bound by shared-memory
+//              bandwidth (8 bytes per two weights): about 26 weights per clock
+//              per SM.  Used for fp32 activations.
+//  LUT_F16MIX  pair table of fp16-rounded levels (relative error <= 2^-12 per
+//              level, well inside the stated 2e-3 bound): one LDS.32 per code
+//              byte halves the shared-memory traffic, and each weight costs one
+//              mixed-precision FMA (f16 x f16 -> f32 accumulate; the product is
+//              exact in fp32).  The thread's x slice is held as fp16 after
+//              scaling by a power of two that puts its largest magnitude in
+//              [2^14, 2^15): bf16 values convert exactly at any magnitude, and
+//              the scale is undone exactly with the block scale.  About 35
+//              weights per clock per SM.  Used for bf16 activations.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -29,7 +37,7 @@
 
 namespace nf4k {
 
-enum LutMode : int { LUT_F32 = 0, LUT_F16 = 1, LUT_F32X2 = 2 };
+enum LutMode : int { LUT_F32 = 0, LUT_F16MIX = 1 };
 
 // Shared-memory plan of one launch (host-computed).
 struct TmaPlan {
@@ -42,39 +50,34 @@ struct TmaPlan {
   int red_off;     // offset of the reduction buffers
 };
 
-template <int LUTM>
-__device__ __forceinline__ float chunk_dot_t(const uint4 c, const float (&xv)[32], uint32_t laneoff,
-                                             const uint8_t* lut) {
+// Two mixed-precision FMAs: acc0 += lo(h) * lo(x), acc1 += hi(h) * hi(x),
+// f16 operands, f32 accumulation.
+__device__ __forceinline__ void fma2_f16_f32(float& acc0, float& acc1, uint32_t h, uint32_t x) {
+  asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+      "mov.b32 {a0, a1}, %2;\n\t"
+      "mov.b32 {b0, b1}, %3;\n\t"
+      "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+      "fma.rn.f32.f16 %1, a1, b1, %1;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(h), "r"(x));
+}
+
+// sum over the 32 weights of one chunk of level(code) * x, fp16 levels and
+// fp16 x pairs (xh[i] holds x[2i] in its low half, x[2i+1] in its high half).
+__device__ __forceinline__ float chunk_dot_f16mix(const uint4 c, const uint32_t (&xh)[16], uint32_t laneoff,
+                                                  const uint8_t* lut) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-  if (LUTM == LUT_F16) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 4; ++q) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t off = __byte_perm(w[q], laneoff, 0x5504u | (j << 4));
-        const __half2 h = *reinterpret_cast<const __half2*>(lut + off);
-        const float2 v = __half22float2(h);
-        acc[j] = fmaf(v.x, xv[8 * q + 2 * j], acc[j]);
-        acc[j] = fmaf(v.y, xv[8 * q + 2 * j + 1], acc[j]);
-      }
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t off = __byte_perm(w[q], laneoff, 0x5504u | (j << 4));
+      const uint32_t h = *reinterpret_cast<const uint32_t*>(lut + off);
+      fma2_f16_f32(acc[2 * j], acc[2 * j + 1], h, xh[4 * q + j]);
     }
-    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
-  } else if (LUTM == LUT_F32X2) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t off = __byte_perm(w[q], laneoff, 0x5504u | (j << 4));
-        const float2 v = *reinterpret_cast<const float2*>(lut + off);
-        ffma2(acc[2 * j], acc[2 * j + 1], v.x, v.y, xv[8 * q + 2 * j], xv[8 * q + 2 * j + 1]);
-      }
-    }
-    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-  } else {
-    return chunk_dot(c, xv, laneoff, lut);
   }
+  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
 template <int NCH, int RB, int EPI, bool XBF16, int LUTM>
@@ -161,7 +164,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
   }
 
   // pair table: byte b, lane l -> (cb[b & 15], cb[b >> 4]) at b * 256 + l * (8 or 4)
-  if (LUTM == LUT_F16) {
+  if (LUTM == LUT_F16MIX) {
     for (int i = tid; i < 256 * 32; i += blockDim.x) {
       const int b = i >> 5, l = i & 31;
       *reinterpret_cast<__half2*>(smem + b * 256 + l * 4) = __floats2half2_rn(cbs[b & 15], cbs[b >> 4]);
@@ -178,14 +181,17 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
   if (is_producer && lane == 0)
     for (; issued < n_it && issued < P.S; ++issued) issue(issued);
 
-  // consumers: x slice to registers
+  // consumers: x slice to registers (fp32, or scaled fp16 pairs for LUT_F16MIX)
   int cidx[NCH];
   bool cval[NCH];
   float xv[NCH][32];
+  uint32_t xh[NCH][16];
+  float xinv[NCH];  // 1 / (power-of-two scale of the fp16 slice)
 #pragma unroll
   for (int j = 0; j < NCH; ++j) {
     cidx[j] = t + G * j;
     cval[j] = !is_producer && cidx[j] < H;
+    xinv[j] = 1.f;
     if (cval[j]) {
       if (XBF16) {
         const uint8_t* xp = reinterpret_cast<const uint8_t*>(a.x) + (int64_t)cidx[j] * 64;
@@ -214,6 +220,24 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
 #pragma unroll
       for (int e = 0; e < 32; ++e) xv[j][e] = 0.f;
     }
+    if (LUTM == LUT_F16MIX) {
+      // largest magnitude of the slice -> scale 2^(14 - e), e its exponent
+      uint32_t mbits = 0;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const uint32_t b = __float_as_uint(xv[j][e]) & 0x7FFFFFFFu;
+        mbits = b > mbits ? b : mbits;
+      }
+      int ex = (int)(mbits >> 23) - 127;
+      ex = ex < -100 ? -100 : ex;
+      const float sig = __uint_as_float((uint32_t)(127 + 14 - ex) << 23);
+      xinv[j] = __uint_as_float((uint32_t)(127 - 14 + ex) << 23);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const __half2 h = __floats2half2_rn(xv[j][2 * e] * sig, xv[j][2 * e + 1] * sig);
+        xh[j][e] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
   }
 
   __syncthreads();
@@ -239,7 +263,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     }
   } else {
     const uint8_t* lut = smem;
-    const uint32_t laneoff = (uint32_t)lane * (LUTM == LUT_F16 ? 4u : 8u);
+    const uint32_t laneoff = (uint32_t)lane * (LUTM == LUT_F16MIX ? 4u : 8u);
     int cidx_c[NCH];
 #pragma unroll
     for (int j = 0; j < NCH; ++j) cidx_c[j] = cval[j] ? cidx[j] : 0;
@@ -277,7 +301,12 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
         for (int i = 0; i < RB; ++i) {
           float r = 0.f;
 #pragma unroll
-          for (int j = 0; j < NCH; ++j) r = fmaf(chunk_dot_t<LUTM>(c[n][i][j], xv[j], laneoff, lut), scl[n][i][j], r);
+          for (int j = 0; j < NCH; ++j) {
+            if (LUTM == LUT_F16MIX)
+              r = fmaf(chunk_dot_f16mix(c[n][i][j], xh[j], laneoff, lut), scl[n][i][j] * xinv[j], r);
+            else
+              r = fmaf(chunk_dot(c[n][i][j], xv[j], laneoff, lut), scl[n][i][j], r);
+          }
           acc[n][i] = r;
         }
       // the stage's shared memory is no longer read by this warp
