@@ -162,7 +162,21 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
     c.nch = 2;
     c.G = 32 * ((H + 63) / 64);
   }
-  c.rb = env_int("NF4_TMA_RB", c.nch == 1 ? 8 : 4);
+  // rows per stage: the largest compiled batch whose stage (all matrices)
+  // stays within 16 KB, so that many stages fit the ring
+  {
+    const int row = nv * (int)(K / 2 + K / 16);
+    const int opts1[] = {8, 4, 2}, opts2[] = {4, 2};
+    const int* opts = c.nch == 1 ? opts1 : opts2;
+    const int nopt = c.nch == 1 ? 3 : 2;
+    c.rb = opts[nopt - 1];
+    for (int i = 0; i < nopt; ++i)
+      if (opts[i] * row <= 16384) {
+        c.rb = opts[i];
+        break;
+      }
+    c.rb = env_int("NF4_TMA_RB", c.rb);
+  }
   // bf16 activations use the fp16-level mixed-precision loop unless NF4_LUT=0
   // asks for the exact fp32 table; fp32 activations always use the fp32 table
   c.lut = env_int("NF4_LUT", LUT_F16MIX) == LUT_F32 ? LUT_F32 : LUT_F16MIX;
@@ -188,7 +202,7 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   if (gpc * c.G + 32 > attr.maxThreadsPerBlock) return c;
   c.gpc = gpc;
   c.threads = gpc * c.G + 32;
-  c.SR = gpc * c.rb;
+  c.SR = c.rb;  // each stage belongs to one row group
   const int row_bytes = (int)(K / 2), srow_bytes = (int)(K / 16);
   c.codes_bytes = c.SR * row_bytes;
   c.scales_bytes = c.SR * srow_bytes;
@@ -196,9 +210,12 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   const int red_bytes = gpc * 2 * nv * c.rb * (c.G / 32) * (int)sizeof(float);
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
-  const int avail = optin - (int)attr.sharedSizeBytes - LUT_BYTES - red_bytes - 8 * 2 * 8 - 256;
+  const int max_stages = 32;
+  const int avail = optin - (int)attr.sharedSizeBytes - LUT_BYTES - red_bytes - 16 * max_stages - 256;
   int S = avail / c.stage_bytes;
-  S = S > env_int("NF4_TMA_STAGES", 6) ? env_int("NF4_TMA_STAGES", 6) : S;
+  const int cap = env_int("NF4_TMA_STAGES", max_stages);
+  S = S > cap ? cap : S;
+  S = S > max_stages ? max_stages : S;
   if (S < 2) return c;
   c.S = S;
   c.bar_off = LUT_BYTES + S * c.stage_bytes;

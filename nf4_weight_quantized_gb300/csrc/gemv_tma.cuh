@@ -3,9 +3,11 @@
 // Same arithmetic and epilogues as gemv_kernel.cuh (source: "Decode V2 --
 // resident executor", section 6 "Linear primitive"), different data movement:
 //  * each block owns a contiguous range of rows, whose codes and scales are
-//    contiguous in memory; one producer thread streams them into a ring of S
-//    shared-memory stages with 1-D cp.async.bulk copies completing on mbarriers
-//    ("full"), marked evict-first in L2 since every weight is read once;
+//    contiguous in memory; one producer thread streams them, RB rows per
+//    stage, into a ring of S shared-memory stages with 1-D cp.async.bulk
+//    copies completing on mbarriers ("full"), marked evict-first in L2 since
+//    every weight is read once; stage i is consumed by row group i % gpc, so
+//    stages stay small however many groups share the block;
 //  * consumer warps are x-stationary as before (thread t of a row group always
 //    owns chunks t + G*j of a row, its x slice lives in registers) and read the
 //    codes of each staged row from shared memory (conflict-free 16-byte loads),
@@ -41,7 +43,7 @@ enum LutMode : int { LUT_F32 = 0, LUT_F16MIX = 1 };
 
 // Shared-memory plan of one launch (host-computed).
 struct TmaPlan {
-  int SR;          // rows per stage (= gpc * RB)
+  int SR;          // rows per stage (= RB)
   int S;           // stages
   int stage_bytes; // bytes of one stage (all matrices: codes then scales)
   int codes_bytes; // SR * K/2, one matrix
@@ -113,7 +115,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
   if (tid == NC) {
     for (int s = 0; s < P.S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), (uint32_t)(NC >> 5));
+      mbar_init(empty_bar(s), (uint32_t)WPG);  // the owning group's warps release it
     }
     mbar_init_fence();
     s_abort = 0;
@@ -269,7 +271,8 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     for (int j = 0; j < NCH; ++j) cidx_c[j] = cval[j] ? cidx[j] : 0;
     float* red = reinterpret_cast<float*>(smem + P.red_off) + group * (2 * NV * RB * WPG);
     int buf = 0;
-    for (int it = 0; it < n_it; ++it) {
+    // stage it belongs to row group it % gpc (round robin)
+    for (int it = group; it < n_it; it += a.gpc) {
       const int s = it % P.S;
       mbar_wait_bounded(full_bar(s), (uint32_t)((it / P.S) & 1), abort);
       const int64_t rb = R0 + (int64_t)it * P.SR;
@@ -286,7 +289,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
         const float* ss = reinterpret_cast<const float*>(st + NV * P.codes_bytes + n * P.scales_bytes);
 #pragma unroll
         for (int i = 0; i < RB; ++i) {
-          const int lr = group * RB + i;
+          const int lr = i;
 #pragma unroll
           for (int j = 0; j < NCH; ++j) {
             c[n][i][j] = lds128(sc + lr * row_bytes + cidx_c[j] * 16);
@@ -320,7 +323,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
       const bool rep = (lane & ((32 >> PL) - 1)) == 0;
       int lr = -1;
       if (WPG == 1) {
-        if (rep) lr = group * RB + rs;
+        if (rep) lr = rs;
       } else {
         float* rbuf = red + buf * (NV * RB * WPG);
         if (rep) {
@@ -329,7 +332,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
         }
         named_bar_sync(1 + group, G);
         if (t < RB) {
-          lr = group * RB + t;
+          lr = t;
 #pragma unroll
           for (int n = 0; n < NV; ++n) {
             float sum = 0.f;

@@ -5,9 +5,9 @@
 
 namespace nf4k {
 
-// Compiled (nch, rb): (1, 4), (1, 8), (2, 2), (2, 4).
+// Compiled (nch, rb): (1, 2), (1, 4), (1, 8), (2, 2), (2, 4).
 inline bool gemv_tma_variant_exists(int nch, int rb) {
-  return (nch == 1 && (rb == 4 || rb == 8)) || (nch == 2 && (rb == 2 || rb == 4));
+  return (nch == 1 && (rb == 2 || rb == 4 || rb == 8)) || (nch == 2 && (rb == 2 || rb == 4));
 }
 
 template <int EPI>
@@ -29,6 +29,7 @@ struct GemvTmaDispatch {
 #define NF4_GEMV_TMA_DEFINE_DISPATCH(E)                                                             \
   template <>                                                                                       \
   const void* GemvTmaDispatch<E>::ptr(int nch, int rb, bool xb, int lut) {                          \
+    NF4_TMA_CASES(NF4_TMA_CASE_L, E, 1, 2)                                                          \
     NF4_TMA_CASES(NF4_TMA_CASE_L, E, 1, 4)                                                          \
     NF4_TMA_CASES(NF4_TMA_CASE_L, E, 1, 8)                                                          \
     NF4_TMA_CASES(NF4_TMA_CASE_L, E, 2, 2)                                                          \
@@ -39,6 +40,7 @@ struct GemvTmaDispatch {
   cudaError_t GemvTmaDispatch<E>::launch(int nch, int rb, bool xb, int lut, const GemvArgs& a,      \
                                          const TmaPlan& p, int blocks, int threads, int smem,       \
                                          cudaStream_t s) {                                          \
+    NF4_TMA_CASES(NF4_TMA_LAUNCH_L, E, 1, 2)                                                        \
     NF4_TMA_CASES(NF4_TMA_LAUNCH_L, E, 1, 4)                                                        \
     NF4_TMA_CASES(NF4_TMA_LAUNCH_L, E, 1, 8)                                                        \
     NF4_TMA_CASES(NF4_TMA_LAUNCH_L, E, 2, 2)                                                        \
