@@ -350,7 +350,7 @@ struct GemvConfig {
 struct TmaConfig {
   bool ok;       // the shape and alignment allow the bulk-copy kernel
   int nch, rb, lut, G, gpc, blocks, threads, smem;
-  int SR, S, stage_bytes, codes_bytes, scales_bytes, bar_off, red_off;
+  int SR, GPS, S, stage_bytes, codes_bytes, scales_bytes, bar_off, red_off;
 };
 TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device);
 cudaError_t launch_gemv_tma(int epi, bool x_bf16, const GemvArgs& a, const TmaConfig& c, cudaStream_t s);

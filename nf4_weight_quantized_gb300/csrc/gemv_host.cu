@@ -162,21 +162,11 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
     c.nch = 2;
     c.G = 32 * ((H + 63) / 64);
   }
-  // rows per stage: the largest compiled batch whose stage (all matrices)
-  // stays within 16 KB, so that many stages fit the ring
-  {
-    const int row = nv * (int)(K / 2 + K / 16);
-    const int opts1[] = {8, 4, 2}, opts2[] = {4, 2};
-    const int* opts = c.nch == 1 ? opts1 : opts2;
-    const int nopt = c.nch == 1 ? 3 : 2;
-    c.rb = opts[nopt - 1];
-    for (int i = 0; i < nopt; ++i)
-      if (opts[i] * row <= 16384) {
-        c.rb = opts[i];
-        break;
-      }
-    c.rb = env_int("NF4_TMA_RB", c.rb);
-  }
+  // rows per group and stage: 4, or 2 when two stages of 4 rows would not
+  // fit beside the pair table (very long rows)
+  c.rb = 4;
+  if (2 * 4 * nv * (int)(K / 2 + K / 16) > 150 * 1024) c.rb = 2;
+  c.rb = env_int("NF4_TMA_RB", c.rb);
   // bf16 activations use the fp16-level mixed-precision loop unless NF4_LUT=0
   // asks for the exact fp32 table; fp32 activations always use the fp32 table
   c.lut = env_int("NF4_LUT", LUT_F16MIX) == LUT_F32 ? LUT_F32 : LUT_F16MIX;
@@ -202,16 +192,28 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   if (gpc * c.G + 32 > attr.maxThreadsPerBlock) return c;
   c.gpc = gpc;
   c.threads = gpc * c.G + 32;
-  c.SR = c.rb;  // each stage belongs to one row group
   const int row_bytes = (int)(K / 2), srow_bytes = (int)(K / 16);
-  c.codes_bytes = c.SR * row_bytes;
-  c.scales_bytes = c.SR * srow_bytes;
-  c.stage_bytes = nv * (c.codes_bytes + c.scales_bytes);
   const int red_bytes = gpc * 2 * nv * c.rb * (c.G / 32) * (int)sizeof(float);
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   const int max_stages = 32;
   const int avail = optin - (int)attr.sharedSizeBytes - LUT_BYTES - red_bytes - 16 * max_stages - 256;
+  // groups per stage: the largest divisor of gpc that still leaves room for
+  // two stages (big block-wide stages stream best; long rows need small ones)
+  const int one_group = nv * c.rb * (row_bytes + srow_bytes);
+  int gps = 1;
+  for (int d = gpc; d >= 1; --d)
+    if (gpc % d == 0 && 2 * d * one_group <= avail) {
+      gps = d;
+      break;
+    }
+  const int gps_env = env_int("NF4_TMA_GPS", 0);
+  if (gps_env > 0 && gpc % gps_env == 0 && 2 * gps_env * one_group <= avail) gps = gps_env;
+  c.GPS = gps;
+  c.SR = gps * c.rb;
+  c.codes_bytes = c.SR * row_bytes;
+  c.scales_bytes = c.SR * srow_bytes;
+  c.stage_bytes = nv * (c.codes_bytes + c.scales_bytes);
   int S = avail / c.stage_bytes;
   const int cap = env_int("NF4_TMA_STAGES", max_stages);
   S = S > cap ? cap : S;
@@ -242,7 +244,7 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
 }
 
 cudaError_t launch_gemv_tma(int epi, bool xb, const GemvArgs& a, const TmaConfig& c, cudaStream_t s) {
-  TmaPlan p{c.SR, c.S, c.stage_bytes, c.codes_bytes, c.scales_bytes, c.bar_off, c.red_off};
+  TmaPlan p{c.SR, c.GPS, c.S, c.stage_bytes, c.codes_bytes, c.scales_bytes, c.bar_off, c.red_off};
   switch (epi) {
     case EPI_PLAIN:
       return GemvTmaDispatch<EPI_PLAIN>::launch(c.nch, c.rb, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);

@@ -6,8 +6,10 @@
 //    contiguous in memory; one producer thread streams them, RB rows per
 //    stage, into a ring of S shared-memory stages with 1-D cp.async.bulk
 //    copies completing on mbarriers ("full"), marked evict-first in L2 since
-//    every weight is read once; stage i is consumed by row group i % gpc, so
-//    stages stay small however many groups share the block;
+//    every weight is read once; a stage holds RB rows for each of GPS row
+//    groups and the stages go round robin over the gpc / GPS sets of groups
+//    (GPS = gpc: every group reads every stage; GPS = 1: small per-group
+//    stages, for long rows or two matrices);
 //  * consumer warps are x-stationary as before (thread t of a row group always
 //    owns chunks t + G*j of a row, its x slice lives in registers) and read the
 //    codes of each staged row from shared memory (conflict-free 16-byte loads),
@@ -43,7 +45,8 @@ enum LutMode : int { LUT_F32 = 0, LUT_F16MIX = 1 };
 
 // Shared-memory plan of one launch (host-computed).
 struct TmaPlan {
-  int SR;          // rows per stage (= RB)
+  int SR;          // rows per stage (= GPS * RB)
+  int GPS;         // row groups sharing one stage (a divisor of gpc)
   int S;           // stages
   int stage_bytes; // bytes of one stage (all matrices: codes then scales)
   int codes_bytes; // SR * K/2, one matrix
@@ -115,7 +118,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
   if (tid == NC) {
     for (int s = 0; s < P.S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), (uint32_t)WPG);  // the owning group's warps release it
+      mbar_init(empty_bar(s), (uint32_t)(P.GPS * WPG));  // the owning groups' warps release it
     }
     mbar_init_fence();
     s_abort = 0;
@@ -271,8 +274,11 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     for (int j = 0; j < NCH; ++j) cidx_c[j] = cval[j] ? cidx[j] : 0;
     float* red = reinterpret_cast<float*>(smem + P.red_off) + group * (2 * NV * RB * WPG);
     int buf = 0;
-    // stage it belongs to row group it % gpc (round robin)
-    for (int it = group; it < n_it; it += a.gpc) {
+    // stage it belongs to the GPS groups of set it % (gpc / GPS); within the
+    // stage, group g reads rows (g % GPS) * RB .. + RB
+    const int sets = a.gpc / P.GPS;
+    const int pos = group % P.GPS;
+    for (int it = group / P.GPS; it < n_it; it += sets) {
       const int s = it % P.S;
       mbar_wait_bounded(full_bar(s), (uint32_t)((it / P.S) & 1), abort);
       const int64_t rb = R0 + (int64_t)it * P.SR;
@@ -289,7 +295,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
         const float* ss = reinterpret_cast<const float*>(st + NV * P.codes_bytes + n * P.scales_bytes);
 #pragma unroll
         for (int i = 0; i < RB; ++i) {
-          const int lr = i;
+          const int lr = pos * RB + i;
 #pragma unroll
           for (int j = 0; j < NCH; ++j) {
             c[n][i][j] = lds128(sc + lr * row_bytes + cidx_c[j] * 16);
@@ -323,7 +329,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
       const bool rep = (lane & ((32 >> PL) - 1)) == 0;
       int lr = -1;
       if (WPG == 1) {
-        if (rep) lr = rs;
+        if (rep) lr = pos * RB + rs;
       } else {
         float* rbuf = red + buf * (NV * RB * WPG);
         if (rep) {
@@ -332,7 +338,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
         }
         named_bar_sync(1 + group, G);
         if (t < RB) {
-          lr = t;
+          lr = pos * RB + t;
 #pragma unroll
           for (int n = 0; n < NV; ++n) {
             float sum = 0.f;
