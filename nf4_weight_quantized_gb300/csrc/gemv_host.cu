@@ -155,7 +155,7 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
     // one warp per row, two chunks per thread: no cross-warp reduction
     c.nch = env_int("NF4_TMA_NCH", 2);
     c.G = c.nch == 2 ? 32 : 64;
-  } else if (32 * ((H + 31) / 32) <= 992) {
+  } else if (32 * ((H + 31) / 32) <= 992 && env_int("NF4_TMA_NCH", 1) == 1) {
     c.nch = 1;
     c.G = 32 * ((H + 31) / 32);
   } else {
@@ -166,6 +166,14 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   // fit beside the pair table (very long rows)
   c.rb = 4;
   if (2 * 4 * nv * (int)(K / 2 + K / 16) > 150 * 1024) c.rb = 2;
+  // two chunks per thread and few rows per block (short kernels): 2 rows per
+  // stage start the computation sooner (measured: 2048 x 2048 and SwiGLU
+  // 11008 x 2048 are faster, lm_head's 151936 rows are not)
+  {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (c.nch == 2 && M < 512LL * (sms > 0 ? sms : 1)) c.rb = 2;
+  }
   c.rb = env_int("NF4_TMA_RB", c.rb);
   // bf16 activations use the fp16-level mixed-precision loop unless NF4_LUT=0
   // asks for the exact fp32 table; fp32 activations always use the fp32 table
