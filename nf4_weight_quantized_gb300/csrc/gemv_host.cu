@@ -195,7 +195,7 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   }
   const int target = env_int("NF4_TMA_THREADS", 768);
   int gpc = (target + c.G / 2) / c.G;
-  gpc = gpc < 1 ? 1 : (gpc > 15 ? 15 : gpc);
+  gpc = gpc < 1 ? 1 : (gpc > 14 ? 14 : gpc);  // named barriers: 1..14 per group, 15 for all consumers
   while (gpc > 1 && gpc * c.G + 32 > attr.maxThreadsPerBlock) --gpc;
   if (gpc * c.G + 32 > attr.maxThreadsPerBlock) return c;
   c.gpc = gpc;

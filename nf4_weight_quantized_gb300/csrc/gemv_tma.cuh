@@ -168,23 +168,31 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     }
   }
 
-  // pair table: byte b, lane l -> (cb[b & 15], cb[b >> 4]) at b * 256 + l * (8 or 4)
-  if (LUTM == LUT_F16MIX) {
-    for (int i = tid; i < 256 * 32; i += blockDim.x) {
-      const int b = i >> 5, l = i & 31;
-      *reinterpret_cast<__half2*>(smem + b * 256 + l * 4) = __floats2half2_rn(cbs[b & 15], cbs[b >> 4]);
-    }
+  // The producer goes straight to its copies (the first bytes are on the
+  // critical path of short kernels); the consumers build the pair table:
+  // byte b, lane l -> (cb[b & 15], cb[b >> 4]) at b * 256 + l * (4 or 8),
+  // written 16 bytes (4 or 2 identical lane replicas) at a time.
+  if (is_producer) {
+    pdl_wait();  // global reads and writes follow the previous kernel's completion
+    if (lane == 0)
+      for (; issued < n_it && issued < P.S; ++issued) issue(issued);
   } else {
-    for (int i = tid; i < 256 * 32; i += blockDim.x) {
-      const int b = i >> 5;
-      reinterpret_cast<float2*>(smem)[i] = make_float2(cbs[b & 15], cbs[b >> 4]);
+    if (LUTM == LUT_F16MIX) {
+      for (int i = tid; i < 256 * 8; i += NC) {
+        const int b = i >> 3, q = i & 7;
+        const __half2 h = __floats2half2_rn(cbs[b & 15], cbs[b >> 4]);
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(&h);
+        *reinterpret_cast<uint4*>(smem + b * 256 + q * 16) = make_uint4(u, u, u, u);
+      }
+    } else {
+      for (int i = tid; i < 256 * 16; i += NC) {
+        const int b = i >> 4, q = i & 15;
+        const uint32_t lo = __float_as_uint(cbs[b & 15]), hi = __float_as_uint(cbs[b >> 4]);
+        *reinterpret_cast<uint4*>(smem + b * 256 + q * 16) = make_uint4(lo, hi, lo, hi);
+      }
     }
+    pdl_wait();
   }
-
-  // everything below reads or writes global memory the previous kernel may own
-  pdl_wait();
-  if (is_producer && lane == 0)
-    for (; issued < n_it && issued < P.S; ++issued) issue(issued);
 
   // consumers: x slice to registers (fp32, or scaled fp16 pairs for LUT_F16MIX)
   int cidx[NCH];
@@ -245,7 +253,8 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     }
   }
 
-  __syncthreads();
+  // consumers only: the pair table is complete (the producer is already busy)
+  if (!is_producer) named_bar_sync(15, NC);
 
   volatile int* abort = &s_abort;
   unsigned long long best = 0ull;
@@ -278,11 +287,22 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     // stage, group g reads rows (g % GPS) * RB .. + RB
     const int sets = a.gpc / P.GPS;
     const int pos = group % P.GPS;
+    // after the warp transpose reduction, lane holds row slot rs; one lane
+    // per slot (rep) carries it on
+    const int rs = (PL == 0) ? 0 : (lane >> (5 - PL));
+    const bool rep = (lane & ((32 >> PL) - 1)) == 0;
     for (int it = group / P.GPS; it < n_it; it += sets) {
       const int s = it % P.S;
       mbar_wait_bounded(full_bar(s), (uint32_t)((it / P.S) & 1), abort);
       const int64_t rb = R0 + (int64_t)it * P.SR;
       const int rows = (int)((R1 - rb) < P.SR ? (R1 - rb) : P.SR);
+      // the residual of the row this thread will write, fetched now so its
+      // latency hides under the stage's arithmetic
+      float resid_v = 0.f;
+      if (EPI == EPI_RESID) {
+        const int my = (WPG == 1) ? (rep ? pos * RB + rs : -1) : (t < RB ? pos * RB + t : -1);
+        if (my >= 0 && my < rows) resid_v = a.resid[rb + my];
+      }
       const uint8_t* st = stages + (size_t)s * P.stage_bytes;
       // Branch-free: every thread computes all RB rows of its group.  Chunks a
       // thread does not own read chunk 0 with x = 0 and add exactly zero; rows
@@ -325,8 +345,6 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
       float v[NV];
 #pragma unroll
       for (int n = 0; n < NV; ++n) v[n] = transpose_reduce<RB>(acc[n], lane);
-      const int rs = (PL == 0) ? 0 : (lane >> (5 - PL));
-      const bool rep = (lane & ((32 >> PL) - 1)) == 0;
       int lr = -1;
       if (WPG == 1) {
         if (rep) lr = pos * RB + rs;
@@ -353,7 +371,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
         if (EPI == EPI_PLAIN) {
           a.y[row] = v[0];
         } else if (EPI == EPI_RESID) {
-          a.y[row] = v[0] + a.resid[row];
+          a.y[row] = v[0] + resid_v;
         } else if (EPI == EPI_SWIGLU) {
           const float g = v[0];
           const float u = v[NV - 1];
