@@ -308,6 +308,11 @@ cudaError_t checked_launch(const void* fn, int threads, int smem, Launch&& launc
   return retry;
 }
 
+// Arrive on a named barrier without waiting (count threads take part).
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

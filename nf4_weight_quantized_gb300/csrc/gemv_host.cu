@@ -201,11 +201,14 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   c.gpc = gpc;
   c.threads = gpc * c.G + 32;
   const int row_bytes = (int)(K / 2), srow_bytes = (int)(K / 16);
-  const int red_bytes = gpc * 2 * nv * c.rb * (c.G / 32) * (int)sizeof(float);
+  // per stage: the stage itself, its two barriers, and one reduction slot
+  // (NV x RB x warps-per-group partial sums) plus a counter per group; one
+  // extra slot set on top (S + 1 slots)
+  const int red_set = gpc * (nv * c.rb * (c.G / 32) * (int)sizeof(float) + (int)sizeof(int));
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   const int max_stages = 32;
-  const int avail = optin - (int)attr.sharedSizeBytes - LUT_BYTES - red_bytes - 16 * max_stages - 256;
+  const int avail = optin - (int)attr.sharedSizeBytes - LUT_BYTES - red_set - 256;
   // groups per stage: the largest divisor of gpc that still leaves room for
   // two stages (big block-wide stages stream best; long rows need small ones)
   const int one_group = nv * c.rb * (row_bytes + srow_bytes);
@@ -222,7 +225,7 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   c.codes_bytes = c.SR * row_bytes;
   c.scales_bytes = c.SR * srow_bytes;
   c.stage_bytes = nv * (c.codes_bytes + c.scales_bytes);
-  int S = avail / c.stage_bytes;
+  int S = avail / (c.stage_bytes + 16 + red_set);
   const int cap = env_int("NF4_TMA_STAGES", max_stages);
   S = S > cap ? cap : S;
   S = S > max_stages ? max_stages : S;
@@ -230,7 +233,7 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   c.S = S;
   c.bar_off = LUT_BYTES + S * c.stage_bytes;
   c.red_off = c.bar_off + 16 * S;
-  c.smem = c.red_off + red_bytes;
+  c.smem = c.red_off + (S + 1) * red_set;
   for (int xb = 0; xb < 2; ++xb)
     cudaFuncSetAttribute(tma_ptr(epi, c.nch, c.rb, xb != 0, lut_for(xb)), cudaFuncAttributeMaxDynamicSharedMemorySize,
                          c.smem);

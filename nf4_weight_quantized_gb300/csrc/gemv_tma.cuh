@@ -115,16 +115,31 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
   auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(P.S + s); };
 
-  if (tid == NC) {
-    for (int s = 0; s < P.S; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), (uint32_t)(P.GPS * WPG));  // the owning groups' warps release it
+  // Reduction slots: per group, S + 1 slots of NV x RB x WPG partial sums and
+  // one arrival counter each (see the stage loop).
+  const int R = P.S + 1;
+  const int slot_floats = NV * RB * WPG;
+  float* red = reinterpret_cast<float*>(smem + P.red_off);
+  int* red_cnt = reinterpret_cast<int*>(smem + P.red_off) + a.gpc * R * slot_floats;
+
+  // Barrier ids: 13 = consumers only, 15 = consumers + producer (initialized
+  // barriers, complete pair table).  The producer never waits on either.
+  if (is_producer) {
+    if (lane == 0) {
+      for (int s = 0; s < P.S; ++s) {
+        mbar_init(full_bar(s), 1);
+        mbar_init(empty_bar(s), (uint32_t)(P.GPS * WPG));  // the owning groups' warps release it
+      }
+      mbar_init_fence();
+      s_abort = 0;
     }
-    mbar_init_fence();
-    s_abort = 0;
+    __syncwarp();
+    named_bar_arrive(15, NC + 32);
+  } else {
+    if (tid < 16) cbs[tid] = a.cb.v[tid];
+    for (int i = tid; i < a.gpc * R; i += NC) red_cnt[i] = 0;
+    named_bar_sync(13, NC);
   }
-  if (tid < 16) cbs[tid] = a.cb.v[tid];
-  __syncthreads();
 
   // producer: issue the first S stages before anything else
   uint64_t policy = 0;
@@ -253,8 +268,8 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     }
   }
 
-  // consumers only: the pair table is complete (the producer is already busy)
-  if (!is_producer) named_bar_sync(15, NC);
+  // consumers: the barriers are initialized and the pair table is complete
+  if (!is_producer) named_bar_sync(15, NC + 32);
 
   volatile int* abort = &s_abort;
   unsigned long long best = 0ull;
@@ -281,8 +296,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     int cidx_c[NCH];
 #pragma unroll
     for (int j = 0; j < NCH; ++j) cidx_c[j] = cval[j] ? cidx[j] : 0;
-    float* red = reinterpret_cast<float*>(smem + P.red_off) + group * (2 * NV * RB * WPG);
-    int buf = 0;
+    int li = 0;  // this group's stage count
     // stage it belongs to the GPS groups of set it % (gpc / GPS); within the
     // stage, group g reads rows (g % GPS) * RB .. + RB
     const int sets = a.gpc / P.GPS;
@@ -300,7 +314,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
       // latency hides under the stage's arithmetic
       float resid_v = 0.f;
       if (EPI == EPI_RESID) {
-        const int my = (WPG == 1) ? (rep ? pos * RB + rs : -1) : (t < RB ? pos * RB + t : -1);
+        const int my = (WPG == 1) ? (rep ? pos * RB + rs : -1) : (lane < RB ? pos * RB + lane : -1);
         if (my >= 0 && my < rows) resid_v = a.resid[rb + my];
       }
       const uint8_t* st = stages + (size_t)s * P.stage_bytes;
@@ -349,23 +363,42 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
       if (WPG == 1) {
         if (rep) lr = pos * RB + rs;
       } else {
-        float* rbuf = red + buf * (NV * RB * WPG);
+        // Every warp leaves its partial sums in the group's slot and counts
+        // itself in; the last warp to arrive adds the WPG partials in warp
+        // order (deterministic) and writes the rows, while the others go on
+        // to their next stage without waiting.  A slot is reused S + 1 stages
+        // later: no warp can get that far ahead of the warp still reducing it,
+        // because the producer refills a stage only after every warp has
+        // released it.
+        float* slot = red + (group * R + li % R) * slot_floats;
+        int* cnt = red_cnt + group * R + li % R;
         if (rep) {
 #pragma unroll
-          for (int n = 0; n < NV; ++n) rbuf[(n * RB + rs) * WPG + wig] = v[n];
+          for (int n = 0; n < NV; ++n) slot[(n * RB + rs) * WPG + wig] = v[n];
         }
-        named_bar_sync(1 + group, G);
-        if (t < RB) {
-          lr = pos * RB + t;
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          __threadfence_block();
+          last = (atomicAdd(cnt, 1) == WPG - 1) ? 1 : 0;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence_block();
+          if (lane < RB) {
+            lr = pos * RB + lane;
 #pragma unroll
-          for (int n = 0; n < NV; ++n) {
-            float sum = 0.f;
-            for (int w = 0; w < WPG; ++w) sum += rbuf[(n * RB + t) * WPG + w];
-            v[n] = sum;
+            for (int n = 0; n < NV; ++n) {
+              float sum = 0.f;
+              for (int w = 0; w < WPG; ++w) sum += slot[(n * RB + lane) * WPG + w];
+              v[n] = sum;
+            }
           }
+          __syncwarp();
+          if (lane == 0) *cnt = 0;
         }
-        buf ^= 1;
       }
+      ++li;
       if (lr >= 0 && lr < rows && !*abort) {
         const int64_t row = rb + lr;
         if (EPI == EPI_PLAIN) {
