@@ -178,26 +178,33 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   // bf16 activations use the fp16-level mixed-precision loop unless NF4_LUT=0
   // asks for the exact fp32 table; fp32 activations always use the fp32 table
   c.lut = env_int("NF4_LUT", LUT_F16MIX) == LUT_F32 ? LUT_F32 : LUT_F16MIX;
-  if (!gemv_tma_variant_exists(c.nch, c.rb)) return c;
   auto lut_for = [&](int xb) { return xb ? c.lut : (int)LUT_F32; };
-  const void* fn = tma_ptr(epi, c.nch, c.rb, true, lut_for(1));
   // both activation-dtype instances share the configuration: take the
-  // tighter thread limit and the larger static shared memory of the two
+  // tighter thread limit and the larger static shared memory of the two;
+  // when a row group does not fit in one block, retry with 2 rows per stage
   cudaFuncAttributes attr{};
-  for (int xb = 0; xb < 2; ++xb) {
-    cudaFuncAttributes ax{};
-    if (cudaFuncGetAttributes(&ax, tma_ptr(epi, c.nch, c.rb, xb != 0, lut_for(xb))) != cudaSuccess) {
-      cudaGetLastError();
-      return c;
+  const void* fn = nullptr;
+  int gpc = 1;
+  for (int attempt = 0;; ++attempt) {
+    if (!gemv_tma_variant_exists(c.nch, c.rb)) return c;
+    fn = tma_ptr(epi, c.nch, c.rb, true, lut_for(1));
+    for (int xb = 0; xb < 2; ++xb) {
+      cudaFuncAttributes ax{};
+      if (cudaFuncGetAttributes(&ax, tma_ptr(epi, c.nch, c.rb, xb != 0, lut_for(xb))) != cudaSuccess) {
+        cudaGetLastError();
+        return c;
+      }
+      if (xb == 0 || ax.maxThreadsPerBlock < attr.maxThreadsPerBlock) attr.maxThreadsPerBlock = ax.maxThreadsPerBlock;
+      if (xb == 0 || ax.sharedSizeBytes > attr.sharedSizeBytes) attr.sharedSizeBytes = ax.sharedSizeBytes;
     }
-    if (xb == 0 || ax.maxThreadsPerBlock < attr.maxThreadsPerBlock) attr.maxThreadsPerBlock = ax.maxThreadsPerBlock;
-    if (xb == 0 || ax.sharedSizeBytes > attr.sharedSizeBytes) attr.sharedSizeBytes = ax.sharedSizeBytes;
+    const int target = env_int("NF4_TMA_THREADS", 768);
+    gpc = (target + c.G / 2) / c.G;
+    gpc = gpc < 1 ? 1 : (gpc > 14 ? 14 : gpc);
+    while (gpc > 1 && gpc * c.G + 32 > attr.maxThreadsPerBlock) --gpc;
+    if (gpc * c.G + 32 <= attr.maxThreadsPerBlock) break;
+    if (c.rb == 2 || attempt > 0) return c;
+    c.rb = 2;
   }
-  const int target = env_int("NF4_TMA_THREADS", 768);
-  int gpc = (target + c.G / 2) / c.G;
-  gpc = gpc < 1 ? 1 : (gpc > 14 ? 14 : gpc);  // named barriers: 1..14 per group, 15 for all consumers
-  while (gpc > 1 && gpc * c.G + 32 > attr.maxThreadsPerBlock) --gpc;
-  if (gpc * c.G + 32 > attr.maxThreadsPerBlock) return c;
   c.gpc = gpc;
   c.threads = gpc * c.G + 32;
   const int row_bytes = (int)(K / 2), srow_bytes = (int)(K / 16);
