@@ -164,8 +164,12 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   }
   // rows per group and stage: 4, or 2 when two stages of 4 rows would not
   // fit beside the pair table (very long rows)
-  c.rb = 4;
-  if (2 * 4 * nv * (int)(K / 2 + K / 16) > 150 * 1024) c.rb = 2;
+  // rows per group and stage: 8 for one-chunk shapes (long per-warp work
+  // amortizes the per-stage reduction; measured best for 2048 x 11008 and
+  // 13824 x 5120), else 4; fewer when two stages would not fit beside the
+  // pair table
+  c.rb = c.nch == 1 ? 8 : 4;
+  while (c.rb > 2 && 2 * c.rb * nv * (int)(K / 2 + K / 16) > 150 * 1024) c.rb /= 2;
   // two chunks per thread and few rows per block (short kernels): 2 rows per
   // stage start the computation sooner (measured: 2048 x 2048 and SwiGLU
   // 11008 x 2048 are faster, lm_head's 151936 rows are not)
@@ -202,8 +206,8 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
     gpc = gpc < 1 ? 1 : (gpc > 14 ? 14 : gpc);
     while (gpc > 1 && gpc * c.G + 32 > attr.maxThreadsPerBlock) --gpc;
     if (gpc * c.G + 32 <= attr.maxThreadsPerBlock) break;
-    if (c.rb == 2 || attempt > 0) return c;
-    c.rb = 2;
+    if (c.rb == 2 || attempt > 2) return c;
+    c.rb /= 2;
   }
   c.gpc = gpc;
   c.threads = gpc * c.G + 32;
