@@ -140,15 +140,17 @@ def bytes_of(kind: str, M: int, K: int, N: int = 1) -> dict:
     return {"weight": w, "total": tot}
 
 
-def build_calls(name: str, torch, nf4, synth, device):
+def build_calls(name: str, torch, nf4, synth, device, copies=None):
     """Inputs for one workload, quantized on the device, with enough rotating
-    weight copies to exceed 3x L2.  Returns (call(i), n_copies, bytes)."""
+    weight copies to exceed 3x L2 (or `copies`).  Returns (call(i), n_copies,
+    bytes, tensors)."""
     w = synth.WORKLOADS[name]
     M, K = w.M, w.K
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 128 << 20)
     b = bytes_of(w.kind, M, K, w.N)
-    copies = max(2, int(np.ceil(3 * l2 / b["weight"])))
+    fixed_copies = copies
+    copies = copies or max(2, int(np.ceil(3 * l2 / b["weight"])))
     d = synth.workload_inputs(w)
 
     def quant(Wnp):
@@ -174,7 +176,7 @@ def build_calls(name: str, torch, nf4, synth, device):
         call = lambda i, s: nf4.nf4_gemv_residual(Ws[i % copies], x, r, y, stream=s)
         ctx = {"W": Ws, "x": x, "r": r, "y": y}
     elif w.kind == "swiglu":
-        copies = max(2, int(np.ceil(3 * l2 / b["weight"])))
+        copies = fixed_copies or max(2, int(np.ceil(3 * l2 / b["weight"])))
         Wg = replicate(quant(d["W"]))
         Wu = replicate(quant(d["Wu"]))
         x = bf16(d["x"])
@@ -429,6 +431,24 @@ def run_gpu(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_target(name: str, calls: int):
+    """Three (or `calls`) untimed calls of one workload, for ncu captures:
+    `ncu ... python bench.py --ncu down_residual`."""
+    import torch
+
+    from nf4_weight_quantized_gb300 import nf4, synth
+
+    device = torch.device("cuda", 0)
+    call, _, b, ctx = build_calls(name, torch, nf4, synth, device, copies=1)
+    s = torch.cuda.current_stream()
+    for i in range(calls):
+        call(0, s)
+    torch.cuda.synchronize()
+    w = synth.WORKLOADS[name]
+    print(json.dumps({"workload": name, "calls": calls, "algorithmic_bytes": b["total"],
+                      "config": nf4.nf4_describe_config(w.M, w.K, w.N)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -440,7 +460,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload-steps", type=int, default=2000)
     ap.add_argument("--no-workloads", dest="all_workloads", action="store_false")
+    ap.add_argument("--ncu", default=None, help="run a few untimed calls of one workload (for ncu) and exit")
+    ap.add_argument("--ncu-calls", type=int, default=3)
     args = ap.parse_args()
+    if args.ncu:
+        run_profile_target(args.ncu, args.ncu_calls)
+        return
     if args.warmup < 3:
         args.warmup = 3
 
