@@ -397,7 +397,7 @@ def run_gpu(args, rank, world, dist):
                     "us_per_call": pc * 1e6, "weight_gbs": b2["weight"] / pc / 1e9,
                     "algorithmic_gbs": b2["total"] / pc / 1e9,
                     "frac_of_hbm": b2["total"] / pc / 1e9 / peaks["hbm_gbs"],
-                    "algorithmic_bytes": b2["total"], "copies": cp2, "calls": n2,
+                    "algorithmic_bytes": b2["total"], "traffic": ncu_traffic(name), "copies": cp2, "calls": n2,
                     "config": nf4.nf4_describe_config(synth.WORKLOADS[name].M, synth.WORKLOADS[name].K,
                                                       synth.WORKLOADS[name].N)}
                 del ctx2, c2
@@ -422,7 +422,7 @@ def run_gpu(args, rank, world, dist):
         "e2e": e2e,
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic("gemv_residual_down"),
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic("down_residual"),
                      "peak_source": peaks["source"], "algorithmic_bytes_per_launch": b["total"]},
         "cpu_baseline": cpu,
     }

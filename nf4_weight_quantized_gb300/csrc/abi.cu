@@ -187,7 +187,7 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
   a.cb = codebook();
   const bool scales16 = aligned(W->scales, 16) && (!W2 || aligned(W2->scales, 16));
   if (scales16 && !use_register_kernel()) {
-    const nf4k::TmaConfig tc = nf4k::choose_tma_config(epi, W->M, W->K, dev);
+    const nf4k::TmaConfig tc = nf4k::choose_tma_config(epi, xt == NF4_BF16, W->M, W->K, dev);
     if (tc.ok) {
       a.G = tc.G;
       a.gpc = tc.gpc;
@@ -387,13 +387,13 @@ const char* nf4_describe_config(int64_t M, int64_t K, int N) {
   }
   char buf[512];
   if (N == 1) {
-    const nf4k::TmaConfig t = use_register_kernel() ? nf4k::TmaConfig{} : nf4k::choose_tma_config(nf4k::EPI_PLAIN, M, K, dev);
+    const nf4k::TmaConfig t = use_register_kernel() ? nf4k::TmaConfig{} : nf4k::choose_tma_config(nf4k::EPI_PLAIN, true, M, K, dev);
     if (t.ok) {
       std::snprintf(buf, sizeof buf,
                     "gemv M=%lld K=%lld (16-byte aligned scales): bulk-copy kernel, %d thread(s) per row, %d row(s) "
                     "per group and stage, %d group(s) (%d per stage) + 1 producer warp per block (%d threads), %d stages of %d rows "
-                    "(%d B), %d blocks, %d B shared memory, %s table, %s",
-                    (long long)M, (long long)K, t.G, t.rb, t.gpc, t.GPS, t.threads, t.S, t.SR, t.stage_bytes, t.blocks,
+                    "(%d B, %d row(s) per full barrier), %d blocks, %d B shared memory, %s table, %s",
+                    (long long)M, (long long)K, t.G, t.rb, t.gpc, t.GPS, t.threads, t.S, t.SR, t.stage_bytes, t.subr, t.blocks,
                     t.smem, t.lut == 1 ? "fp16-level mixed-precision loop for bf16 x" : "fp32 pair",
                     nf4k::pdl_enabled() ? "programmatic dependent launch" : "plain launch");
     } else {

@@ -356,8 +356,10 @@ struct TmaConfig {
   bool ok;       // the shape and alignment allow the bulk-copy kernel
   int nch, rb, lut, G, gpc, blocks, threads, smem;
   int SR, GPS, S, stage_bytes, codes_bytes, scales_bytes, bar_off, red_off;
+  int sub;       // rows per full barrier within a group's rb rows (compiled variant)
+  int subr, nb;  // rows per full barrier in the stage, full barriers per stage
 };
-TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device);
+TmaConfig choose_tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int device);
 cudaError_t launch_gemv_tma(int epi, bool x_bf16, const GemvArgs& a, const TmaConfig& c, cudaStream_t s);
 
 // Host launchers (gemv.cu / quantize.cu).

@@ -7,6 +7,7 @@
 // sharing one row, set by K), the batch RB (rows in flight per thread) and the
 // number of groups per block, with the grid sized to fill all SMs once
 // (persistent blocks, each owning a contiguous range of rows).
+#include <algorithm>
 #include <cstdlib>
 #include <map>
 #include <mutex>
@@ -56,12 +57,12 @@ std::mutex g_mu;
 std::map<Key, GemvConfig> g_cache;
 std::map<Key, TmaConfig> g_tma_cache;
 
-const void* tma_ptr(int epi, int nch, int rb, bool xb, int lut) {
+const void* tma_ptr(int epi, int nch, int rb, int sub, bool xb, int lut) {
   switch (epi) {
-    case EPI_PLAIN: return GemvTmaDispatch<EPI_PLAIN>::ptr(nch, rb, xb, lut);
-    case EPI_RESID: return GemvTmaDispatch<EPI_RESID>::ptr(nch, rb, xb, lut);
-    case EPI_SWIGLU: return GemvTmaDispatch<EPI_SWIGLU>::ptr(nch, rb, xb, lut);
-    default: return GemvTmaDispatch<EPI_ARGMAX>::ptr(nch, rb, xb, lut);
+    case EPI_PLAIN: return GemvTmaDispatch<EPI_PLAIN>::ptr(nch, rb, sub, xb, lut);
+    case EPI_RESID: return GemvTmaDispatch<EPI_RESID>::ptr(nch, rb, sub, xb, lut);
+    case EPI_SWIGLU: return GemvTmaDispatch<EPI_SWIGLU>::ptr(nch, rb, sub, xb, lut);
+    default: return GemvTmaDispatch<EPI_ARGMAX>::ptr(nch, rb, sub, xb, lut);
   }
 }
 
@@ -134,12 +135,66 @@ GemvConfig choose_gemv_config(int epi, int64_t M, int64_t K, int device) {
   return c;
 }
 
+// Groups of G threads per block for the bulk-copy kernel, from a cost model
+// of the busiest group: blocks take ceil(M / blocks) rows each, in stages of
+// GPS x RB rows handed round robin to the gpc / GPS sets of groups, and a
+// block's groups share the SM's arithmetic, so the block's time goes as
+// (stages of the busiest set) x RB x gpc.  Blocks keep at least 8 compute
+// warps; ties go to the count nearest 768 compute threads.  (Measured on
+// 13824 x 5120: 4 groups of 160 threads, 2 per stage, 12.3 us; 5 groups, 1 per
+// stage, whose last stages leave three groups idle, 13.4 us.)
+int tma_groups_per_stage(int gpc, int G, int rb, int nv, int64_t K, const cudaFuncAttributes& attr, int device);
+
+int pick_groups(int G, int rb, int nv, int64_t M, int64_t K, const cudaFuncAttributes& attr, int device) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  sms = sms > 0 ? sms : 1;
+  const int max_threads = attr.maxThreadsPerBlock < 1024 ? attr.maxThreadsPerBlock : 1024;
+  int gcap = (max_threads - 32) / G;
+  gcap = gcap > 14 ? 14 : gcap;
+  if (gcap < 1) return 0;
+  int gmin = (256 + G - 1) / G;
+  gmin = gmin > gcap ? gcap : gmin;
+  int64_t cost[15] = {0};
+  int64_t min_cost = -1;
+  for (int g = gmin; g <= gcap; ++g) {
+    const int d = tma_groups_per_stage(g, G, rb, nv, K, attr, device);
+    const int64_t SR = (int64_t)d * rb;
+    const int64_t blocks = std::min<int64_t>((M + SR - 1) / SR, sms);
+    const int64_t rows = (M + blocks - 1) / blocks;
+    const int64_t n_it = (rows + SR - 1) / SR;
+    const int64_t sets = g / d;
+    cost[g] = ((n_it + sets - 1) / sets) * rb * g;
+    if (min_cost < 0 || cost[g] < min_cost) min_cost = cost[g];
+  }
+  // within 2% of the cheapest counts as a tie
+  int best = 0;
+  for (int g = gmin; g <= gcap; ++g)
+    if (cost[g] * 50 <= min_cost * 51 && (best == 0 || std::abs(g * G - 768) < std::abs(best * G - 768))) best = g;
+  return best;
+}
+
+// Groups per stage: the largest divisor of gpc whose stages still fit twice
+// beside the pair table and the reduction slots (big block-wide stages stream
+// best; long rows need small ones).
+int tma_groups_per_stage(int gpc, int G, int rb, int nv, int64_t K, const cudaFuncAttributes& attr, int device) {
+  int optin = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  const int red_set = gpc * (nv * rb * (G / 32) * (int)sizeof(float) + (int)sizeof(int));
+  const int avail = optin - (int)attr.sharedSizeBytes - LUT_BYTES - red_set - 256;
+  const int one_group = nv * rb * (int)(K / 2 + K / 16);
+  for (int d = gpc; d >= 1; --d)
+    if (gpc % d == 0 && 2 * d * one_group <= avail) return d;
+  return 1;
+}
+
 // Bulk-copy kernel: x-stationary row groups as in the register kernel, plus a
 // producer warp and a ring of S stages of SR rows each, one block per SM.
-TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
+TmaConfig choose_tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int device) {
+  const int key_epi = 2 * epi + (x_bf16 ? 1 : 0);
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_tma_cache.find(Key{epi, device, M, K});
+    auto it = g_tma_cache.find(Key{key_epi, device, M, K});
     if (it != g_tma_cache.end()) return it->second;
   }
   TmaConfig c{};
@@ -183,29 +238,32 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   // asks for the exact fp32 table; fp32 activations always use the fp32 table
   c.lut = env_int("NF4_LUT", LUT_F16MIX) == LUT_F32 ? LUT_F32 : LUT_F16MIX;
   auto lut_for = [&](int xb) { return xb ? c.lut : (int)LUT_F32; };
-  // both activation-dtype instances share the configuration: take the
-  // tighter thread limit and the larger static shared memory of the two;
-  // when a row group does not fit in one block, retry with 2 rows per stage
+  // each activation dtype has its own instance and configuration (their
+  // register use differs); when a row group does not fit in one block, retry
+  // with fewer rows per stage
+  const int xb = x_bf16 ? 1 : 0;
   cudaFuncAttributes attr{};
   const void* fn = nullptr;
   int gpc = 1;
   for (int attempt = 0;; ++attempt) {
-    if (!gemv_tma_variant_exists(c.nch, c.rb)) return c;
-    fn = tma_ptr(epi, c.nch, c.rb, true, lut_for(1));
-    for (int xb = 0; xb < 2; ++xb) {
-      cudaFuncAttributes ax{};
-      if (cudaFuncGetAttributes(&ax, tma_ptr(epi, c.nch, c.rb, xb != 0, lut_for(xb))) != cudaSuccess) {
-        cudaGetLastError();
-        return c;
-      }
-      if (xb == 0 || ax.maxThreadsPerBlock < attr.maxThreadsPerBlock) attr.maxThreadsPerBlock = ax.maxThreadsPerBlock;
-      if (xb == 0 || ax.sharedSizeBytes > attr.sharedSizeBytes) attr.sharedSizeBytes = ax.sharedSizeBytes;
+    // rows per full barrier within a group's rows: all of them unless asked
+    c.sub = env_int("NF4_TMA_SUB", c.rb);
+    if (!gemv_tma_variant_exists(c.nch, c.rb, c.sub)) c.sub = c.rb;
+    if (!gemv_tma_variant_exists(c.nch, c.rb, c.sub)) return c;
+    fn = tma_ptr(epi, c.nch, c.rb, c.sub, x_bf16, lut_for(xb));
+    if (fn == nullptr || cudaFuncGetAttributes(&attr, fn) != cudaSuccess) {
+      cudaGetLastError();
+      return c;
     }
-    const int target = env_int("NF4_TMA_THREADS", 768);
-    gpc = (target + c.G / 2) / c.G;
-    gpc = gpc < 1 ? 1 : (gpc > 14 ? 14 : gpc);
-    while (gpc > 1 && gpc * c.G + 32 > attr.maxThreadsPerBlock) --gpc;
-    if (gpc * c.G + 32 <= attr.maxThreadsPerBlock) break;
+    const int env_threads = env_int("NF4_TMA_THREADS", 0);
+    if (env_threads > 0) {
+      gpc = (env_threads + c.G / 2) / c.G;
+      gpc = gpc < 1 ? 1 : (gpc > 14 ? 14 : gpc);
+      while (gpc > 1 && gpc * c.G + 32 > attr.maxThreadsPerBlock) --gpc;
+    } else {
+      gpc = pick_groups(c.G, c.rb, nv, M, K, attr, device);
+    }
+    if (gpc >= 1 && gpc * c.G + 32 <= attr.maxThreadsPerBlock) break;
     if (c.rb == 2 || attempt > 2) return c;
     c.rb /= 2;
   }
@@ -220,34 +278,50 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   const int max_stages = 32;
   const int avail = optin - (int)attr.sharedSizeBytes - LUT_BYTES - red_set - 256;
-  // groups per stage: the largest divisor of gpc that still leaves room for
-  // two stages (big block-wide stages stream best; long rows need small ones)
   const int one_group = nv * c.rb * (row_bytes + srow_bytes);
-  int gps = 1;
-  for (int d = gpc; d >= 1; --d)
-    if (gpc % d == 0 && 2 * d * one_group <= avail) {
-      gps = d;
-      break;
-    }
+  int gps = tma_groups_per_stage(gpc, c.G, c.rb, nv, K, attr, device);
   const int gps_env = env_int("NF4_TMA_GPS", 0);
   if (gps_env > 0 && gpc % gps_env == 0 && 2 * gps_env * one_group <= avail) gps = gps_env;
   c.GPS = gps;
   c.SR = gps * c.rb;
+  // When every group gets a single stage (few rows per block, long rows),
+  // split its rows over two full barriers so it can start on the first half
+  // while the second is in flight (measured on 2048 x 11008: 6.6 us against
+  // 6.9 us; with several stages per group the split costs more than it saves)
+  if (env_int("NF4_TMA_SUB", 0) == 0 && c.rb >= 4 && gemv_tma_variant_exists(c.nch, c.rb, c.rb / 2)) {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    const int64_t blocks_est = std::min<int64_t>((M + c.SR - 1) / c.SR, sms > 0 ? sms : 1);
+    const int64_t rows_pb = (M + blocks_est - 1) / blocks_est;
+    const int64_t per_group = ((rows_pb + c.SR - 1) / c.SR + (gpc / gps) - 1) / (gpc / gps);
+    const void* half = tma_ptr(epi, c.nch, c.rb, c.rb / 2, x_bf16, lut_for(xb));
+    cudaFuncAttributes ah{};
+    if (per_group <= 1 && half != nullptr && cudaFuncGetAttributes(&ah, half) == cudaSuccess &&
+        ah.maxThreadsPerBlock >= c.threads && ah.sharedSizeBytes == attr.sharedSizeBytes) {
+      c.sub = c.rb / 2;
+      fn = half;
+    }
+    cudaGetLastError();
+  }
+  // rows per full barrier: SUB when a group's rows are split (the consumers
+  // start on the first rows of a stage while the rest are in flight), else
+  // one barrier for the whole stage
+  c.subr = c.sub < c.rb ? c.sub : c.SR;
+  c.nb = c.SR / c.subr;
+  const int bars_bytes = 8 * (c.nb + 1);  // per stage
   c.codes_bytes = c.SR * row_bytes;
   c.scales_bytes = c.SR * srow_bytes;
   c.stage_bytes = nv * (c.codes_bytes + c.scales_bytes);
-  int S = avail / (c.stage_bytes + 16 + red_set);
+  int S = (avail - 16) / (c.stage_bytes + bars_bytes + red_set);
   const int cap = env_int("NF4_TMA_STAGES", max_stages);
   S = S > cap ? cap : S;
   S = S > max_stages ? max_stages : S;
   if (S < 2) return c;
   c.S = S;
   c.bar_off = LUT_BYTES + S * c.stage_bytes;
-  c.red_off = c.bar_off + 16 * S;
+  c.red_off = (c.bar_off + bars_bytes * S + 15) / 16 * 16;
   c.smem = c.red_off + (S + 1) * red_set;
-  for (int xb = 0; xb < 2; ++xb)
-    cudaFuncSetAttribute(tma_ptr(epi, c.nch, c.rb, xb != 0, lut_for(xb)), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         c.smem);
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, c.smem);
   int sms = 0, bps = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, c.threads, c.smem);
@@ -261,21 +335,21 @@ TmaConfig choose_tma_config(int epi, int64_t M, int64_t K, int device) {
   c.ok = true;
   cudaGetLastError();
   std::lock_guard<std::mutex> lk(g_mu);
-  g_tma_cache[Key{epi, device, M, K}] = c;
+  g_tma_cache[Key{key_epi, device, M, K}] = c;
   return c;
 }
 
 cudaError_t launch_gemv_tma(int epi, bool xb, const GemvArgs& a, const TmaConfig& c, cudaStream_t s) {
-  TmaPlan p{c.SR, c.GPS, c.S, c.stage_bytes, c.codes_bytes, c.scales_bytes, c.bar_off, c.red_off};
+  TmaPlan p{c.SR, c.GPS, c.S, c.stage_bytes, c.codes_bytes, c.scales_bytes, c.bar_off, c.red_off, c.subr, c.nb};
   switch (epi) {
     case EPI_PLAIN:
-      return GemvTmaDispatch<EPI_PLAIN>::launch(c.nch, c.rb, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
+      return GemvTmaDispatch<EPI_PLAIN>::launch(c.nch, c.rb, c.sub, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
     case EPI_RESID:
-      return GemvTmaDispatch<EPI_RESID>::launch(c.nch, c.rb, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
+      return GemvTmaDispatch<EPI_RESID>::launch(c.nch, c.rb, c.sub, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
     case EPI_SWIGLU:
-      return GemvTmaDispatch<EPI_SWIGLU>::launch(c.nch, c.rb, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
+      return GemvTmaDispatch<EPI_SWIGLU>::launch(c.nch, c.rb, c.sub, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
     default:
-      return GemvTmaDispatch<EPI_ARGMAX>::launch(c.nch, c.rb, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
+      return GemvTmaDispatch<EPI_ARGMAX>::launch(c.nch, c.rb, c.sub, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
   }
 }
 

@@ -9,7 +9,9 @@
 //    every weight is read once; a stage holds RB rows for each of GPS row
 //    groups and the stages go round robin over the gpc / GPS sets of groups
 //    (GPS = gpc: every group reads every stage; GPS = 1: small per-group
-//    stages, for long rows or two matrices);
+//    stages, for long rows or two matrices); a stage's rows complete on NB
+//    "full" barriers of SUBR rows each, so the consumers start on the first
+//    rows of a large stage while the rest are still in flight;
 //  * consumer warps are x-stationary as before (thread t of a row group always
 //    owns chunks t + G*j of a row, its x slice lives in registers) and read the
 //    codes of each staged row from shared memory (conflict-free 16-byte loads),
@@ -51,8 +53,10 @@ struct TmaPlan {
   int stage_bytes; // bytes of one stage (all matrices: codes then scales)
   int codes_bytes; // SR * K/2, one matrix
   int scales_bytes;// SR * K/64 * 4, one matrix
-  int bar_off;     // offset of the 2*S mbarriers
+  int bar_off;     // offset of the S*(NB+1) mbarriers
   int red_off;     // offset of the reduction buffers
+  int SUBR;        // rows per full barrier: SUB, or SR (one per stage)
+  int NB;          // full barriers per stage (SR / SUBR)
 };
 
 // Two mixed-precision FMAs: acc0 += lo(h) * lo(x), acc1 += hi(h) * hi(x),
@@ -85,8 +89,9 @@ __device__ __forceinline__ float chunk_dot_f16mix(const uint4 c, const uint32_t 
   return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
-template <int NCH, int RB, int EPI, bool XBF16, int LUTM>
+template <int NCH, int RB, int SUB, int EPI, bool XBF16, int LUTM>
 __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid_constant__ TmaPlan P) {
+  static_assert(SUB >= 1 && RB % SUB == 0, "SUB rows per full barrier must divide RB");
   constexpr int NV = (EPI == EPI_SWIGLU) ? 2 : 1;
   constexpr int PL = Log2<RB>::value;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -111,9 +116,10 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
   const int nblk = a.K >> 6;
 
   uint8_t* stages = smem + LUT_BYTES;
-  const uint32_t bar0 = smem_addr(smem + P.bar_off);  // full[s] at bar0 + 8s, empty[s] at bar0 + 8(S+s)
-  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(P.S + s); };
+  // full[s][b] at bar0 + 8(s NB + b), empty[s] at bar0 + 8(S NB + s)
+  const uint32_t bar0 = smem_addr(smem + P.bar_off);
+  auto full_bar = [&](int s, int b) { return bar0 + 8u * (uint32_t)(s * P.NB + b); };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(P.S * P.NB + s); };
 
   // Reduction slots: per group, S + 1 slots of NV x RB x WPG partial sums and
   // one arrival counter each (see the stage loop).
@@ -127,7 +133,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
   if (is_producer) {
     if (lane == 0) {
       for (int s = 0; s < P.S; ++s) {
-        mbar_init(full_bar(s), 1);
+        for (int b = 0; b < P.NB; ++b) mbar_init(full_bar(s, b), 1);
         mbar_init(empty_bar(s), (uint32_t)(P.GPS * WPG));  // the owning groups' warps release it
       }
       mbar_init_fence();
@@ -151,19 +157,33 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     mcodes[NV - 1] = a.codes2;
     mscales[NV - 1] = a.scales2;
   }
+  // one stage: per full barrier, the codes and scales of its SUBR rows (rows
+  // are contiguous in memory and in the stage, so one copy per matrix each);
+  // a barrier whose rows lie past the block's end is completed by a plain
+  // arrival, so every barrier completes every phase
   auto issue = [&](int it) {
     const int s = it % P.S;
     const int64_t rb = R0 + (int64_t)it * P.SR;
     const int rows = (int)((R1 - rb) < P.SR ? (R1 - rb) : P.SR);
-    const uint32_t cb = (uint32_t)rows * (uint32_t)row_bytes;
-    const uint32_t sb = (uint32_t)rows * (uint32_t)nblk * 4u;
-    mbar_arrive_expect_tx(full_bar(s), NV * (cb + sb));
     uint8_t* st = stages + (size_t)s * P.stage_bytes;
+    for (int b = 0; b < P.NB; ++b) {
+      const int r0 = b * P.SUBR;
+      const int nr = rows - r0 < P.SUBR ? rows - r0 : P.SUBR;
+      const uint32_t fb = full_bar(s, b);
+      if (nr <= 0) {
+        mbar_arrive(fb);
+        continue;
+      }
+      const uint32_t cb = (uint32_t)nr * (uint32_t)row_bytes;
+      const uint32_t sb = (uint32_t)nr * (uint32_t)nblk * 4u;
+      mbar_arrive_expect_tx(fb, NV * (cb + sb));
 #pragma unroll
-    for (int n = 0; n < NV; ++n) {
-      bulk_g2s(smem_addr(st + n * P.codes_bytes), mcodes[n] + rb * row_bytes, cb, full_bar(s), policy);
-      bulk_g2s(smem_addr(st + NV * P.codes_bytes + n * P.scales_bytes), mscales[n] + rb * nblk, sb,
-               full_bar(s), policy);
+      for (int n = 0; n < NV; ++n) {
+        bulk_g2s(smem_addr(st + n * P.codes_bytes + r0 * row_bytes), mcodes[n] + (rb + r0) * row_bytes, cb, fb,
+                 policy);
+        bulk_g2s(smem_addr(st + NV * P.codes_bytes + n * P.scales_bytes + r0 * nblk * 4),
+                 mscales[n] + (rb + r0) * nblk, sb, fb, policy);
+      }
     }
   };
   // Before the previous kernel on the stream has finished (programmatic
@@ -286,8 +306,9 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
         // drain: wait (bounded, ignoring the abort flag) for every copy that
         // may still be in flight, so none lands after the block has exited
         for (int it = (issued > P.S ? issued - P.S : 0); it < issued; ++it)
-          for (uint32_t i = 0; i < kWaitPolls; ++i)
-            if (mbar_try_wait(full_bar(it % P.S), (uint32_t)((it / P.S) & 1))) break;
+          for (int b = 0; b < P.NB; ++b)
+            for (uint32_t i = 0; i < kWaitPolls; ++i)
+              if (mbar_try_wait(full_bar(it % P.S, b), (uint32_t)((it / P.S) & 1))) break;
       }
     }
   } else {
@@ -307,7 +328,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     const bool rep = (lane & ((32 >> PL) - 1)) == 0;
     for (int it = group / P.GPS; it < n_it; it += sets) {
       const int s = it % P.S;
-      mbar_wait_bounded(full_bar(s), (uint32_t)((it / P.S) & 1), abort);
+      const uint32_t par = (uint32_t)((it / P.S) & 1);
       const int64_t rb = R0 + (int64_t)it * P.SR;
       const int rows = (int)((R1 - rb) < P.SR ? (R1 - rb) : P.SR);
       // the residual of the row this thread will write, fetched now so its
@@ -321,37 +342,43 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
       // Branch-free: every thread computes all RB rows of its group.  Chunks a
       // thread does not own read chunk 0 with x = 0 and add exactly zero; rows
       // past the end of the last stage compute garbage that is never stored.
-      uint4 c[NV][RB][NCH];
-      float scl[NV][RB][NCH];
-#pragma unroll
-      for (int n = 0; n < NV; ++n) {
-        const uint8_t* sc = st + n * P.codes_bytes;
-        const float* ss = reinterpret_cast<const float*>(st + NV * P.codes_bytes + n * P.scales_bytes);
-#pragma unroll
-        for (int i = 0; i < RB; ++i) {
-          const int lr = pos * RB + i;
-#pragma unroll
-          for (int j = 0; j < NCH; ++j) {
-            c[n][i][j] = lds128(sc + lr * row_bytes + cidx_c[j] * 16);
-            scl[n][i][j] = ss[lr * nblk + (cidx_c[j] >> 1)];
-          }
-        }
-      }
+      // The group's RB rows are taken SUB at a time: wait for the full barrier
+      // that covers them, read all their codes and scales (the loads issue
+      // back to back), then multiply them out.
       float acc[NV][RB];
 #pragma unroll
-      for (int n = 0; n < NV; ++n)
+      for (int sb = 0; sb < RB / SUB; ++sb) {
+        const int lr0 = pos * RB + sb * SUB;
+        mbar_wait_bounded(full_bar(s, lr0 / P.SUBR), par, abort);
+        uint4 c[NV][SUB][NCH];
+        float scl[NV][SUB][NCH];
 #pragma unroll
-        for (int i = 0; i < RB; ++i) {
-          float r = 0.f;
+        for (int n = 0; n < NV; ++n) {
+          const uint8_t* sc = st + n * P.codes_bytes;
+          const float* ss = reinterpret_cast<const float*>(st + NV * P.codes_bytes + n * P.scales_bytes);
 #pragma unroll
-          for (int j = 0; j < NCH; ++j) {
-            if (LUTM == LUT_F16MIX)
-              r = fmaf(chunk_dot_f16mix(c[n][i][j], xh[j], laneoff, lut), scl[n][i][j] * xinv[j], r);
-            else
-              r = fmaf(chunk_dot(c[n][i][j], xv[j], laneoff, lut), scl[n][i][j], r);
-          }
-          acc[n][i] = r;
+          for (int i = 0; i < SUB; ++i)
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+              c[n][i][j] = lds128(sc + (lr0 + i) * row_bytes + cidx_c[j] * 16);
+              scl[n][i][j] = ss[(lr0 + i) * nblk + (cidx_c[j] >> 1)];
+            }
         }
+#pragma unroll
+        for (int n = 0; n < NV; ++n)
+#pragma unroll
+          for (int i = 0; i < SUB; ++i) {
+            float r = 0.f;
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+              if (LUTM == LUT_F16MIX)
+                r = fmaf(chunk_dot_f16mix(c[n][i][j], xh[j], laneoff, lut), scl[n][i][j] * xinv[j], r);
+              else
+                r = fmaf(chunk_dot(c[n][i][j], xv[j], laneoff, lut), scl[n][i][j], r);
+            }
+            acc[n][sb * SUB + i] = r;
+          }
+      }
       // the stage's shared memory is no longer read by this warp
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(s));
@@ -448,15 +475,15 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
   }
 }
 
-template <int NCH, int RB, int EPI, bool XBF16, int LUTM>
+template <int NCH, int RB, int SUB, int EPI, bool XBF16, int LUTM>
 const void* gemv_tma_ptr() {
-  return reinterpret_cast<const void*>(&gemv_tma_kernel<NCH, RB, EPI, XBF16, LUTM>);
+  return reinterpret_cast<const void*>(&gemv_tma_kernel<NCH, RB, SUB, EPI, XBF16, LUTM>);
 }
 
-template <int NCH, int RB, int EPI, bool XBF16, int LUTM>
+template <int NCH, int RB, int SUB, int EPI, bool XBF16, int LUTM>
 cudaError_t launch_gemv_tma_instance(const GemvArgs& a, const TmaPlan& p, int blocks, int threads, int smem,
                                      cudaStream_t s) {
-  return checked_launch(gemv_tma_ptr<NCH, RB, EPI, XBF16, LUTM>(), threads, smem, [&] {
+  return checked_launch(gemv_tma_ptr<NCH, RB, SUB, EPI, XBF16, LUTM>(), threads, smem, [&] {
     // one wave of persistent blocks: the next kernel may launch early
     // (programmatic dependent launch) and overlap its prologue with our tail
     cudaLaunchConfig_t cfg{};
@@ -469,7 +496,7 @@ cudaError_t launch_gemv_tma_instance(const GemvArgs& a, const TmaPlan& p, int bl
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    cudaLaunchKernelEx(&cfg, gemv_tma_kernel<NCH, RB, EPI, XBF16, LUTM>, a, p);
+    cudaLaunchKernelEx(&cfg, gemv_tma_kernel<NCH, RB, SUB, EPI, XBF16, LUTM>, a, p);
   });
 }
 
