@@ -235,12 +235,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_kernel(const __grid_constan
     if (s_last) {
       __threadfence();
       const int rows = (a.M - m0) < TILE_M ? (a.M - m0) : TILE_M;
-      for (int i = tid; i < a.N * rows; i += NTHREADS) {
-        const int n = i / rows, rr = i - n * rows;
-        const int64_t off = (int64_t)n * a.M + m0 + rr;
-        float sum = 0.f;
-        for (int p = 0; p < a.P; ++p) sum += __ldcg(a.partial + (int64_t)p * a.N * a.M + off);
-        if (!*abort) a.Y[off] = sum;
+      // eight outputs per thread at a time, every partial loaded before any
+      // store (independent loads, not one round trip per output); parts added
+      // in order
+      constexpr int OB = 8;
+      for (int i0 = tid * OB; i0 < a.N * rows; i0 += NTHREADS * OB) {
+        float sum[OB];
+#pragma unroll
+        for (int o = 0; o < OB; ++o) sum[o] = 0.f;
+        for (int p = 0; p < a.P; ++p) {
+          float v[OB];
+#pragma unroll
+          for (int o = 0; o < OB; ++o) {
+            const int i = i0 + o;
+            const int n = i / rows, rr = i - n * rows;
+            v[o] = i < a.N * rows ? __ldcg(a.partial + (int64_t)p * a.N * a.M + (int64_t)n * a.M + m0 + rr) : 0.f;
+          }
+#pragma unroll
+          for (int o = 0; o < OB; ++o) sum[o] += v[o];
+        }
+#pragma unroll
+        for (int o = 0; o < OB; ++o) {
+          const int i = i0 + o;
+          const int n = i / rows, rr = i - n * rows;
+          if (i < a.N * rows && !*abort) a.Y[(int64_t)n * a.M + m0 + rr] = sum[o];
+        }
       }
       if (tid == 0) a.tickets[tile] = 0u;  // leave the workspace zeroed
     }
@@ -267,20 +286,43 @@ int choose_parts(int M, int K, int sms = 152) {
   return best;
 }
 
+size_t fallback_partial_bytes(int64_t M, int64_t K, int N) {
+  const int P = choose_parts((int)M, (int)K);
+  return P <= 1 ? 0 : (size_t)P * N * M * 4;
+}
+
 }  // namespace
 
+// chunk_tma.cu: the stream-K kernel, used when K % 256 == 0 and the operands
+// are 16-byte aligned; this file's kernel serves every other shape.
+bool chunk_tma_usable(int64_t K, const void* codes, const void* scales, const void* X);
+size_t chunk_tma_partial_bytes(int64_t M, int64_t K, int N);
+cudaError_t launch_chunk_tma(const uint8_t* codes, const float* scales, int M, int K, const uint16_t* X, int N,
+                             float* Y, float* partial, unsigned int* tickets, const Codebook& cb, cudaStream_t s);
+std::string describe_chunk_tma(int64_t M, int64_t K, int N);
+
+// Workspace layout, either kernel: split-tile partials from the start, one
+// ticket per 128-row tile at the end followed by 16 spare bytes.  Sized for
+// the larger of the two kernels' needs (which one runs also depends on the
+// pointers' alignment, not known here); split plans are made for a 152-SM
+// GB300 on every device, so the size depends only on the shape.
 size_t chunk_workspace_bytes(int64_t M, int64_t K, int N) {
-  // the partial tiles of the split-K path plus one ticket per row tile; the
-  // split is chosen for a 152-SM GB300 and never exceeds this bound
-  const int P = choose_parts((int)M, (int)K);
-  if (P <= 1) return 16;
+  const size_t a = fallback_partial_bytes(M, K, N), b = chunk_tma_partial_bytes(M, K, N);
+  const size_t part = a > b ? a : b;
+  if (part == 0) return 16;
   const int64_t tiles = (M + TILE_M - 1) / TILE_M;
-  const int64_t part_bytes = (int64_t)P * N * M * 4;
-  return (size_t)(((part_bytes + 255) / 256) * 256 + tiles * 4 + 16);
+  return ((part + 255) / 256) * 256 + (size_t)tiles * 4 + 16;
 }
 
 cudaError_t launch_chunk(const uint8_t* codes, const float* scales, int M, int K, const uint16_t* X, int N, float* Y,
                          void* workspace, const Codebook& cb, cudaStream_t s, int device) {
+  const size_t ws_bytes = chunk_workspace_bytes(M, K, N);
+  const int64_t tiles_all = (M + TILE_M - 1) / TILE_M;
+  unsigned int* tickets =
+      ws_bytes > 16 ? reinterpret_cast<unsigned int*>(reinterpret_cast<uint8_t*>(workspace) + ws_bytes - 16 - tiles_all * 4)
+                    : nullptr;
+  if (chunk_tma_usable(K, codes, scales, X))
+    return launch_chunk_tma(codes, scales, M, K, X, N, Y, reinterpret_cast<float*>(workspace), tickets, cb, s);
   ChunkArgs a{};
   a.codes = codes;
   a.scales = scales;
@@ -293,9 +335,8 @@ cudaError_t launch_chunk(const uint8_t* codes, const float* scales, int M, int K
   (void)device;
   a.P = choose_parts(M, K);
   if (a.P > 1) {
-    const int64_t part_bytes = (int64_t)a.P * N * M * 4;
     a.partial = reinterpret_cast<float*>(workspace);
-    a.tickets = reinterpret_cast<unsigned int*>(reinterpret_cast<uint8_t*>(workspace) + ((part_bytes + 255) / 256) * 256);
+    a.tickets = tickets;
   }
   a.S = 4;
   const int smem = LUT_BYTES + a.S * STAGE_BYTES;
@@ -306,6 +347,7 @@ cudaError_t launch_chunk(const uint8_t* codes, const float* scales, int M, int K
 
 std::string describe_chunk(int64_t M, int64_t K, int N, int device) {
   (void)device;
+  if (K % 256 == 0) return describe_chunk_tma(M, K, N) + " (16-byte aligned operands)";
   const int P = choose_parts((int)M, (int)K);
   char buf[256];
   std::snprintf(buf, sizeof buf,

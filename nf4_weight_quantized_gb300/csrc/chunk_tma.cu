@@ -1,0 +1,605 @@
+// chunk_tma.cu -- prefill chunk (N <= 32 tokens), persistent stream-K kernel fed
+// by the tensor-memory-access (TMA) engine.
+//
+// Y[n][m] = sum_k X[n][k] * bf16(W_hat[m][k]), fp32 accumulation, the same
+// definition as chunk.cu (source: "Decode V2 -- resident executor", section 0
+// item 1 and section 5: prompt chunks of up to 32 tokens through the
+// tensor-core GEMM, each weight read once per chunk).  This kernel is the one
+// used when K is a multiple of 256 and the operands are 16-byte aligned:
+//
+//  * work units are (128-row tile, 256-column slice) pairs, tile-major; each of
+//    min(units, 152) persistent blocks takes one contiguous, equal share of them
+//    (stream-K), so every SM streams the same number of bytes;
+//  * one producer thread loads each unit with 2-D TMA copies: the codes (128 rows
+//    x 128 bytes, 128-byte swizzled so the dequantizing threads read them without
+//    bank conflicts), the 128 x 4 fp32 scales, and the four 64-column slices of X
+//    (32 rows, rows >= N zero-filled by the copy, already in the swizzled K-major
+//    layout the tensor core reads), into a ring of four stages;
+//  * sixteen dequantizing warps turn each 64-column k-tile of codes into the bf16
+//    A operand (fp32 level x fp32 scale from the lane-replicated pair table,
+//    rounded once) and store it straight into tensor memory (tcgen05.st; row m
+//    in TMEM lane m), a ring of three stages of two k-tiles: the A operand never passes
+//    through shared memory, which the pair-table reads alone keep busy;
+//  * one thread issues tcgen05.mma (M = 128, N = 32, K = 16, A from TMEM, X from
+//    shared memory) into one of two 32-column TMEM accumulators, so four
+//    epilogue warps can drain one tile while the next accumulates;
+//  * a tile whose K range is split over several blocks is finished by the last of
+//    them to arrive (a per-tile ticket), which adds the partial tiles in block
+//    order: the result does not depend on timing.
+// Every wait is bounded; on a timeout the block stops issuing work, waits for its
+// copies and tensor-core operations, frees its TMEM and reports the error word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "gemv_kernel.cuh"
+
+namespace nf4k {
+
+namespace {
+
+constexpr int TM = 128;        // MMA M: rows of W per tile
+constexpr int TN = 32;         // MMA N: tokens
+constexpr int KT = 64;         // columns per k-tile (one NF4 block, one swizzle atom of bf16)
+constexpr int KQ = 4;          // k-tiles per unit (256 columns, 128 code bytes per row)
+constexpr int NDQ = 16;        // dequantizing warps
+constexpr int EPI_WARPS = 4;   // warps 0-3: epilogue (TMEM lanes 32w .. 32w + 31)
+constexpr int PROD_WARP = 4;
+constexpr int MMA_WARP = 5;
+constexpr int DQ_WARP0 = 6;
+constexpr int NTHREADS = (DQ_WARP0 + NDQ) * 32;  // 704
+#ifndef NF4_CHUNK_SR
+#define NF4_CHUNK_SR 4
+#endif
+#ifndef NF4_CHUNK_SA
+#define NF4_CHUNK_SA 3
+#endif
+#ifndef NF4_DQ_SLEEP
+#define NF4_DQ_SLEEP 64
+#endif
+constexpr int SR = NF4_CHUNK_SR;  // raw stages (units) in shared memory
+constexpr int SA = NF4_CHUNK_SA;  // A stages in tensor memory, KS k-tiles each
+// k-tiles per A stage: one barrier wait, KS x 4 MMAs and one commit per stage.
+// Measured alone, a wait + fence costs about 190 cycles and a commit 44
+// against 45 per M=128 N=32 K=16 MMA, so one handshake per k-tile would cost
+// more than the k-tile's tensor-core work.
+constexpr int KS = 2;
+static_assert(KQ % KS == 0, "A stages tile a unit");
+constexpr int CODES_BYTES = TM * KQ * KT / 2;    // 16 KB
+constexpr int XT_BYTES = TN * KT * 2;            // 4 KB per k-tile
+constexpr int SCL_BYTES = TM * KQ * 4;           // 2 KB
+constexpr int RAW_BYTES = CODES_BYTES + KQ * XT_BYTES + SCL_BYTES;  // 34 KB
+constexpr int SMEM_BYTES = LUT_BYTES + SR * RAW_BYTES;
+static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory per block");
+// TMEM columns: two 32-column fp32 accumulators, then SA A stages of KS x 32
+// columns (64 bf16 of each row per k-tile, two per 32-bit column)
+constexpr int A_COLS = KS * KT / 2;
+constexpr int A_COL0 = 2 * TN;
+constexpr int TMEM_COLS = 256;
+static_assert(A_COL0 + SA * A_COLS <= TMEM_COLS, "tensor memory per block");
+constexpr int PLAN_SMS = 152;  // blocks planned for a 152-SM GB300 (the workspace depends on the shape only)
+
+static_assert(RAW_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+static_assert(NDQ == 16, "four dequantizing warps per 32-lane quarter of the tile, 16 columns each");
+
+struct StreamKArgs {
+  float* Y;
+  float* partial;         // [tiles][maxseg][N][128]
+  unsigned int* tickets;  // [tiles]
+  int M, K, N;
+  int tiles, NQ;          // row tiles, units per tile (K / 256)
+  long long U;            // units = tiles * NQ
+  int B;                  // blocks
+  int maxseg;             // partial slots per tile (0: whole tiles per block)
+};
+
+// First unit of block b: an equal share of the units, or, when there are at
+// least four tiles per block, an equal share of whole tiles (no tile is split,
+// no partials).
+__host__ __device__ inline long long unit_start(long long b, const StreamKArgs& a) {
+  return a.maxseg == 0 ? (b * a.tiles / a.B) * a.NQ : b * a.U / a.B;
+}
+
+// the block whose unit range holds unit u
+__host__ __device__ inline int block_of(long long u, const StreamKArgs& a) {
+  long long b = u * a.B / a.U;
+  while (b + 1 < a.B && unit_start(b + 1, a) <= u) ++b;
+  while (b > 0 && unit_start(b, a) > u) --b;
+  return (int)b;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint2 lds64(const void* p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p)));
+  return v;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, bf16 inputs, fp32 accumulate; A is
+// M rows in TMEM lanes, each row's K values packed two per 32-bit column.
+__device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-wide store of 8 consecutive 32-bit columns into this warp's 32 TMEM
+// lanes (lane l of the warp writes TMEM lane base + l).
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+// Non-blocking test of a barrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded spin on a barrier phase with the non-blocking test, for the MMA
+// issuer, which is the critical path and should see a phase the moment it
+// completes.
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < 64u * kWaitPolls; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*abort) return false;
+  }
+  *abort = 1;
+  atomicOr(&g_nf4_device_error, kErrWaitTimeout);
+  return false;
+}
+
+// Bounded wait that sleeps `ns` nanoseconds between polls (waits that are long
+// by design leave the barrier unit to the threads on the critical path).
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t ns) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (ns) __nanosleep(ns);
+  }
+  *abort = 1;
+  atomicOr(&g_nf4_device_error, kErrWaitTimeout);
+  return false;
+}
+
+// Warp-wide wait: lane 0 polls, the other lanes wait at the warp barrier, which
+// orders their later accesses after the phase lane 0 observed (one poller per
+// warp instead of 32).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort, int lane,
+                                               uint32_t ns) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait_sleep(bar, parity, abort, ns) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    chunk_tma_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
+                     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ StreamKArgs a,
+                     const __grid_constant__ Codebook cbk) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ float cbs[16];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ unsigned int s_last;
+  __shared__ unsigned long long s_bar[2 * SR + 2 * SA + 4 + 1];
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const long long u0 = unit_start(blockIdx.x, a);
+  const long long u1 = unit_start(blockIdx.x + 1, a);
+  const int nq = (int)(u1 - u0);
+
+  uint8_t* raw0 = smem + LUT_BYTES;
+  const uint32_t bar0 = smem_addr(&s_bar[0]);
+  auto raw_full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto raw_empty = [&](int s) { return bar0 + 8u * (uint32_t)(SR + s); };
+  auto a_full = [&](int s) { return bar0 + 8u * (uint32_t)(2 * SR + s); };
+  auto a_empty = [&](int s) { return bar0 + 8u * (uint32_t)(2 * SR + SA + s); };
+  auto acc_full = [&](int b) { return bar0 + 8u * (uint32_t)(2 * SR + 2 * SA + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (uint32_t)(2 * SR + 2 * SA + 2 + b); };
+  const uint32_t mma_done = bar0 + 8u * (uint32_t)(2 * SR + 2 * SA + 4);
+
+  if (tid == 0) {
+    for (int s = 0; s < SR; ++s) {
+      mbar_init(raw_full(s), 1);
+      mbar_init(raw_empty(s), NDQ + 1);  // the dequantizing warps and the MMA commit
+    }
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(a_full(s), NDQ);
+      mbar_init(a_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    mbar_init_fence();
+    s_abort = 0;
+  }
+  if (tid < 16) cbs[tid] = cbk.v[tid];
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_addr(&s_tmem), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == PROD_WARP && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_codes) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_scales) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_x) : "memory");
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  // producer: one unit = the codes, the four X slices and the scales of a
+  // 128-row x 256-column slice, all completing on the stage's full barrier
+  auto issue_unit = [&](int q) {
+    const int s = q % SR;
+    const long long u = u0 + q;
+    const int tile = (int)(u / a.NQ), kq = (int)(u % a.NQ);
+    uint8_t* raw = raw0 + s * RAW_BYTES;
+    mbar_arrive_expect_tx(raw_full(s), RAW_BYTES);
+    tma_load_2d(smem_addr(raw), &tm_codes, kq * 128, tile * TM, raw_full(s));
+#pragma unroll
+    for (int i = 0; i < KQ; ++i)
+      tma_load_2d(smem_addr(raw + CODES_BYTES + i * XT_BYTES), &tm_x, (kq * KQ + i) * KT, 0, raw_full(s));
+    tma_load_2d(smem_addr(raw + CODES_BYTES + KQ * XT_BYTES), &tm_scales, kq * KQ, tile * TM, raw_full(s));
+  };
+  // the first stages go out before the pair table is built, so the table
+  // build hides under their latency
+  const int pre = (smem_addr(raw0) & 1023u) == 0 ? (nq < SR ? nq : SR) : 0;
+  if (warp == PROD_WARP && lane == 0)
+    for (int q = 0; q < pre; ++q) issue_unit(q);
+  // pair table: byte b, lane l -> (cb[b & 15], cb[b >> 4]) at b * 256 + l * 8
+  for (int i = tid; i < LUT_BYTES / 8; i += NTHREADS) {
+    const int b = i >> 5;
+    reinterpret_cast<float2*>(smem)[i] = make_float2(cbs[b & 15], cbs[b >> 4]);
+  }
+  if (tid == 0 && (smem_addr(raw0) & 1023u) != 0) {  // swizzled tiles need 1024-byte alignment
+    s_abort = 1;
+    atomicOr(&g_nf4_device_error, kErrWaitTimeout);
+  }
+  __syncthreads();
+  volatile int* abort = &s_abort;
+
+  if (warp == PROD_WARP) {
+    // ------------------------------------------------------------ producer
+    // The whole warp runs the loop; lane 0 issues.
+    int issued = pre;
+    for (int q = pre; q < nq; ++q) {
+      const int s = q % SR;
+      if (q >= SR && !mbar_wait_warp(raw_empty(s), (uint32_t)(((q / SR) - 1) & 1), abort, lane, 64)) break;
+      if (__any_sync(0xffffffffu, *abort != 0)) break;  // warp-uniform
+      if (lane == 0) issue_unit(q);
+      __syncwarp();
+      issued = q + 1;
+    }
+    if (*abort && lane == 0) {
+      // wait (bounded, ignoring the flag) for the copies still in flight
+      for (int q = (issued > SR ? issued - SR : 0); q < issued; ++q)
+        for (uint32_t i = 0; i < kWaitPolls; ++i)
+          if (mbar_try_wait(raw_full(q % SR), (uint32_t)((q / SR) & 1))) break;
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    // -------------------------------------------------------- MMA issuer
+    // the whole warp runs the loop, lane 0 issues the tensor-core operations
+    {
+      const uint32_t idesc = idesc_bf16_f32(TM, TN);
+      int j = 0, g = 0;
+      for (int q = 0; q < nq;) {
+        const long long tile = (u0 + q) / a.NQ;
+        const int qs = q;
+        const int qe = (int)((tile + 1) * a.NQ - u0 < nq ? (tile + 1) * a.NQ - u0 : nq);
+        const int buf = g & 1;
+        if (g >= 2) mbar_wait_warp(acc_empty(buf), (uint32_t)(((g >> 1) - 1) & 1), abort, lane, 0);
+        tc_fence_after_sync();
+        const uint32_t dtm = tmem + (uint32_t)(buf * TN);
+        for (; q < qe; ++q) {
+          const int s = q % SR;
+          mbar_wait_warp(raw_full(s), (uint32_t)((q / SR) & 1), abort, lane, 0);
+          const uint32_t xb = smem_addr(raw0 + s * RAW_BYTES + CODES_BYTES);
+          for (int h = 0; h < KQ / KS; ++h, ++j) {
+            const int as = j % SA;
+            mbar_wait_warp(a_full(as), (uint32_t)((j / SA) & 1), abort, lane, 0);
+            tc_fence_after_sync();
+            if (lane == 0) {
+              if (!*abort) {
+                const uint32_t at = tmem + (uint32_t)(A_COL0 + as * A_COLS);
+#pragma unroll
+                for (int i2 = 0; i2 < KS; ++i2)
+#pragma unroll
+                  for (int kk = 0; kk < KT / 16; ++kk)
+                    tc_mma_bf16_ta(dtm, at + i2 * (KT / 2) + kk * 8,
+                                   smem_desc_sw128(xb + (h * KS + i2) * XT_BYTES + kk * 32), idesc,
+                                   (q > qs || h > 0 || i2 > 0 || kk > 0) ? 1u : 0u);
+              }
+              tc_commit(a_empty(as));
+            }
+            __syncwarp();
+          }
+          if (lane == 0) tc_commit(raw_empty(s));  // X of this unit is read once these MMAs complete
+          __syncwarp();
+        }
+        if (lane == 0) tc_commit(acc_full(buf));
+        __syncwarp();
+        ++g;
+      }
+      // every tensor-core operation has completed before TMEM is freed
+      if (lane == 0) {
+        tc_commit(mma_done);
+        for (uint32_t i = 0; i < kWaitPolls; ++i)
+          if (mbar_try_wait(mma_done, 0)) break;
+      }
+      __syncwarp();
+    }
+  } else if (warp >= DQ_WARP0) {
+    // ---------------------------------------------------- dequantization
+    // A warp may reach only TMEM lanes 32 (warp % 4) .. + 31, so each thread owns
+    // one tile row (its TMEM lane) and a 16-column group of every k-tile (the
+    // four warps of a lane quarter take the four groups).
+    const int r = 32 * (warp & 3) + lane;          // tile row = TMEM lane
+    const int cg = (warp - DQ_WARP0) >> 2;         // column group: code bytes 8cg .. 8cg + 7
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t laneoff = (uint32_t)lane * 8u;  // pair-table replica
+    int j = 0;
+    for (int q = 0; q < nq; ++q) {
+      const int s = q % SR;
+      mbar_wait_warp(raw_full(s), (uint32_t)((q / SR) & 1), abort, lane, NF4_DQ_SLEEP);
+      const uint8_t* raw = raw0 + s * RAW_BYTES;
+      const float4 sc4 = *reinterpret_cast<const float4*>(raw + CODES_BYTES + KQ * XT_BYTES + r * 16);
+      const float scl[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+#pragma unroll
+      for (int h = 0; h < KQ / KS; ++h, ++j) {
+        const int as = j % SA;
+        uint32_t p[KS][8];
+#pragma unroll
+        for (int i2 = 0; i2 < KS; ++i2) {
+          const int i = h * KS + i2;
+          const uint2 cw = lds64(raw + r * 128 + (((2 * i + (cg >> 1)) ^ (r & 7)) << 4) + (cg & 1) * 8);
+          const uint32_t w2[2] = {cw.x, cw.y};
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const uint32_t off = __byte_perm(w2[e], laneoff, 0x5504u | (jj << 4));
+              const float2 v = *reinterpret_cast<const float2*>(smem + off);
+              p[i2][4 * e + jj] = pack_bf16x2(v.x * scl[i], v.y * scl[i]);
+            }
+        }
+        // the tensor core has finished with this A stage's previous contents
+        if (j >= SA) mbar_wait_warp(a_empty(as), (uint32_t)(((j / SA) - 1) & 1), abort, lane, NF4_DQ_SLEEP);
+        tc_fence_after_sync();
+#pragma unroll
+        for (int i2 = 0; i2 < KS; ++i2)
+          tmem_st_32x32b_x8(tmem + lane_base + (uint32_t)(A_COL0 + as * A_COLS + i2 * (KT / 2) + cg * 8), p[i2]);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a_full(as));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(raw_empty(s));
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int er = warp * 32 + lane;  // tile row = TMEM lane
+    int g = 0;
+    for (int q = 0; q < nq; ++g) {
+      const long long tile = (u0 + q) / a.NQ;
+      const int qe = (int)((tile + 1) * a.NQ - u0 < nq ? (tile + 1) * a.NQ - u0 : nq);
+      q = qe;
+      const int buf = g & 1;
+      const bool ok = mbar_wait_warp(acc_full(buf), (uint32_t)((g >> 1) & 1), abort, lane, 128);
+      tc_fence_after_sync();
+      uint32_t acc[32];
+      tmem_ld_32x32b_x32(tmem + (uint32_t)(buf * TN) + ((uint32_t)(warp * 32) << 16), acc);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(buf));
+      const long long m = tile * TM + er;
+      const int bf = a.maxseg == 0 ? (int)blockIdx.x : block_of(tile * a.NQ, a);
+      const int nseg = a.maxseg == 0 ? 1 : block_of(tile * a.NQ + a.NQ - 1, a) - bf + 1;
+      if (nseg == 1) {
+        if (ok && !*abort && m < a.M) {
+#pragma unroll
+          for (int n = 0; n < TN; ++n)
+            if (n < a.N) a.Y[(long long)n * a.M + m] = __uint_as_float(acc[n]);
+        }
+        continue;
+      }
+      // partial tile: the last of the tile's blocks to arrive adds all of them in block order
+      const int si = (int)blockIdx.x - bf;
+      float* slot = a.partial + ((long long)tile * a.maxseg + si) * a.N * TM;
+      if (ok && !*abort) {
+#pragma unroll
+        for (int n = 0; n < TN; ++n)
+          if (n < a.N) slot[n * TM + er] = __uint_as_float(acc[n]);
+      }
+      __threadfence();
+      named_bar_sync(1, EPI_WARPS * 32);
+      if (tid == 0) {
+        const unsigned int prev = atomicAdd(&a.tickets[tile], 1u);
+        s_last = (prev == (unsigned int)nseg - 1) ? 1u : 0u;
+      }
+      named_bar_sync(1, EPI_WARPS * 32);
+      if (s_last) {
+        __threadfence();
+        // all of a slot's values are loaded before any store (32 independent
+        // loads per slot, not one round trip per value); slots added in order
+        const float* base = a.partial + (long long)tile * a.maxseg * a.N * TM;
+        float sum[TN];
+#pragma unroll
+        for (int n = 0; n < TN; ++n) sum[n] = 0.f;
+        for (int k = 0; k < nseg; ++k) {
+          float v[TN];
+#pragma unroll
+          for (int n = 0; n < TN; ++n) v[n] = n < a.N ? __ldcg(base + ((long long)k * a.N + n) * TM + er) : 0.f;
+#pragma unroll
+          for (int n = 0; n < TN; ++n) sum[n] += v[n];
+        }
+        if (!*abort && m < a.M) {
+#pragma unroll
+          for (int n = 0; n < TN; ++n)
+            if (n < a.N) a.Y[(long long)n * a.M + m] = sum[n];
+        }
+        if (tid == 0) a.tickets[tile] = 0u;  // leave the workspace zeroed
+      }
+      named_bar_sync(1, EPI_WARPS * 32);  // s_last is read before the next tile rewrites it
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiled encode_fn() {
+  static std::once_flag once;
+  static EncodeTiled fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+struct Plan {
+  int tiles, NQ, B, maxseg;
+  long long U;
+};
+
+Plan plan_for(int64_t M, int64_t K) {
+  Plan p{};
+  p.tiles = (int)((M + TM - 1) / TM);
+  p.NQ = (int)(K / (KT * KQ));
+  p.U = (long long)p.tiles * p.NQ;
+  p.B = (int)(p.U < PLAN_SMS ? p.U : PLAN_SMS);
+  if (p.B < 1) p.B = 1;
+  if (p.tiles >= 4 * p.B) {  // whole tiles per block: at most 1 tile in 4 of imbalance
+    p.maxseg = 0;
+    return p;
+  }
+  const long long min_units = p.U / p.B;  // >= 1
+  long long ms = (p.NQ + min_units - 1) / min_units + 1;
+  p.maxseg = (int)(ms < p.B ? ms : p.B);
+  return p;
+}
+
+}  // namespace
+
+bool chunk_tma_usable(int64_t K, const void* codes, const void* scales, const void* X) {
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  return K % (KT * KQ) == 0 && a16(codes) && a16(scales) && a16(X) && encode_fn() != nullptr;
+}
+
+// Bytes of the split-tile partials (tickets are placed by the caller).
+size_t chunk_tma_partial_bytes(int64_t M, int64_t K, int N) {
+  if (K % (KT * KQ) != 0) return 0;
+  const Plan p = plan_for(M, K);
+  return (size_t)p.tiles * (size_t)p.maxseg * N * TM * sizeof(float);
+}
+
+cudaError_t launch_chunk_tma(const uint8_t* codes, const float* scales, int M, int K, const uint16_t* X, int N,
+                             float* Y, float* partial, unsigned int* tickets, const Codebook& cb, cudaStream_t s) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const Plan p = plan_for(M, K);
+  CUtensorMap mc, ms, mx;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+    const cuuint32_t box[2] = {128, TM};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)K / 64, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K / 64 * 4};
+    const cuuint32_t box[2] = {KQ, TM};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(scales), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {KT, TN};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  StreamKArgs a{};
+  a.Y = Y;
+  a.partial = partial;
+  a.tickets = tickets;
+  a.M = M;
+  a.K = K;
+  a.N = N;
+  a.tiles = p.tiles;
+  a.NQ = p.NQ;
+  a.U = p.U;
+  a.B = p.B;
+  a.maxseg = p.maxseg;
+  return checked_launch(reinterpret_cast<const void*>(&chunk_tma_kernel), NTHREADS, SMEM_BYTES, [&] {
+    chunk_tma_kernel<<<p.B, NTHREADS, SMEM_BYTES, s>>>(mc, ms, mx, a, cb);
+  });
+}
+
+std::string describe_chunk_tma(int64_t M, int64_t K, int N) {
+  const Plan p = plan_for(M, K);
+  char buf[320];
+  std::snprintf(buf, sizeof buf,
+                "chunk M=%lld K=%lld N=%d: tcgen05 M=%d N=%d K=16, %s over %lld units of 128 rows x 256 "
+                "columns on %d persistent blocks (%d threads: %d dequantizing warps, TMA producer, MMA issuer, 4 "
+                "epilogue warps), %d raw + %d operand stages, 2 TMEM accumulators",
+                (long long)M, (long long)K, N, TM, TN, p.maxseg == 0 ? "whole tiles per block" : "stream-K", p.U, p.B,
+                NTHREADS, NDQ, SR, SA);
+  return buf;
+}
+
+}  // namespace nf4k

@@ -109,3 +109,31 @@ def test_chunk_zero_level_rows(nf4):
     X = synth.normal_bf16(620, 1, N * K).reshape(N, K)
     Y, _ = _run(nf4, codes, scales, X)
     assert np.all(Y == 0.0)
+
+
+def test_chunk_kernel_choice_is_described(nf4):
+    # K % 256 == 0: the stream-K TMA kernel (whole tiles per block when there are
+    # at least four tiles per block); other K: the register-fed kernel
+    assert "stream-K" in nf4.nf4_describe_config(13824, 5120, 32)
+    assert "whole tiles per block" in nf4.nf4_describe_config(81920, 256, 5)
+    assert "stream-K" not in nf4.nf4_describe_config(1000, 192, 4)
+
+
+def test_chunk_whole_tiles_per_block(nf4):
+    # 640 row tiles on 152 blocks: no tile is split, no partials
+    M, K, N = 81920 + 40, 256, 5
+    codes, scales = H.quantized(630, 0, M, K)
+    X = synth.normal_bf16(630, 1, N * K).reshape(N, K)
+    Y, _ = _run(nf4, codes, scales, X)
+    _check(Y, codes, scales, X, what="whole tiles")
+
+
+@pytest.mark.parametrize("M,K,N", [(384, 256, 32), (129, 768, 3), (1536, 2816, 17)])
+def test_chunk_stream_k_ragged(nf4, M, K, N):
+    # units of 256 columns split unevenly over the blocks, ragged last tile
+    codes, scales = H.quantized(640 + M, 0, M, K)
+    X = synth.normal_bf16(640 + M, 1, N * K).reshape(N, K)
+    Y, ws = _run(nf4, codes, scales, X)
+    _check(Y, codes, scales, X, what=f"stream-K {M}x{K} N={N}")
+    Y2, _ = _run(nf4, codes, scales, X, ws)
+    assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
