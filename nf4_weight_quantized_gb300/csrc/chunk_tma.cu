@@ -144,30 +144,13 @@ __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
-// Non-blocking test of a barrier phase.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded spin on a barrier phase with the non-blocking test, for the MMA
-// issuer, which is the critical path and should see a phase the moment it
-// completes.
-__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < 64u * kWaitPolls; ++i) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if (*abort) return false;
-  }
-  *abort = 1;
-  atomicOr(&g_nf4_device_error, kErrWaitTimeout);
-  return false;
+// (r0, r1) = (a0 * b, a1 * b), each product rounded to nearest even: one
+// packed fp32 multiply instead of two.
+__device__ __forceinline__ void mul2_f32(float& r0, float& r1, float a0, float a1, float b) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b));
 }
 
 // Bounded wait that sleeps `ns` nanoseconds between polls (waits that are long
@@ -390,7 +373,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int jj = 0; jj < 4; ++jj) {
               const uint32_t off = __byte_perm(w2[e], laneoff, 0x5504u | (jj << 4));
               const float2 v = *reinterpret_cast<const float2*>(smem + off);
-              p[i2][4 * e + jj] = pack_bf16x2(v.x * scl[i], v.y * scl[i]);
+              float w0, w1;
+              mul2_f32(w0, w1, v.x, v.y, scl[i]);  // two IEEE products, as v.x * s and v.y * s
+              p[i2][4 * e + jj] = pack_bf16x2(w0, w1);
             }
         }
         // the tensor core has finished with this A stage's previous contents
