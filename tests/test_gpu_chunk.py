@@ -137,3 +137,27 @@ def test_chunk_stream_k_ragged(nf4, M, K, N):
     _check(Y, codes, scales, X, what=f"stream-K {M}x{K} N={N}")
     Y2, _ = _run(nf4, codes, scales, X, ws)
     assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
+
+
+def test_chunk_fallback_kernel_unaligned_scales(nf4):
+    # K % 256 == 0 but scales only 4-byte aligned: the register-fed kernel
+    # (P-way split-K) runs instead of the TMA one; same definition, same bound
+    M, K, N = 1000, 1024, 13
+    codes, scales = H.quantized(650, 0, M, K)
+    W = H.weight_tensors(codes, scales)
+    buf = torch.zeros(scales.size + 4, dtype=torch.float32, device="cuda")
+    buf[1:1 + scales.size].copy_(torch.from_numpy(scales.reshape(-1)))
+    Wu = nf4.NF4Weight(W.codes, buf[1:1 + scales.size].view(M, K // 64))
+    assert Wu.scales.data_ptr() % 16 == 4
+    X = synth.normal_bf16(650, 1, N * K).reshape(N, K)
+    Xt = H.bf16_tensor(X.reshape(-1)).view(N, K)
+    ws = nf4.new_workspace(M, K, N)
+    Y = torch.full((N, M), 777.0, device="cuda")
+    nf4.nf4_gemm_chunk(Wu, Xt, Y, workspace=ws)
+    _check(Y.cpu().numpy(), codes, scales, X, what="fallback chunk")
+    Y2 = torch.full((N, M), 777.0, device="cuda")
+    nf4.nf4_gemm_chunk(W, Xt, Y2, workspace=ws)  # aligned: the TMA kernel, same workspace
+    _check(Y2.cpu().numpy(), codes, scales, X, what="TMA chunk after fallback")
+    nb = nf4.nf4_workspace_bytes(M, K, N)
+    tail = ws[:nb].view(torch.uint8)[-((M + 127) // 128) * 4 - 16:]
+    assert torch.count_nonzero(tail).item() == 0
