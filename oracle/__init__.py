@@ -45,6 +45,7 @@ def load():
     lib.nf4o_gemv_swiglu.argtypes = [P, P, P, P, I64, I64, P, I, P, I64, P, P, P, P]
     lib.nf4o_gemv_argmax.argtypes = [P, P, I64, I64, P, I, P, P, P]
     lib.nf4o_gemm_chunk.argtypes = [P, P, I64, I64, P, I64, P, I64, P, P]
+    lib.nf4o_gemv_qkv.argtypes = [P, P, P, P, I64, P, I, P, I64, P, P]
     lib.nf4o_round_bf16.argtypes = [ctypes.c_double]
     lib.nf4o_round_bf16.restype = ctypes.c_uint16
     for name in ("nf4o_codebook", "nf4o_quantize", "nf4o_dequant", "nf4o_gemv", "nf4o_gemv_residual",
@@ -129,6 +130,28 @@ def gemv_residual(codes, scales, x, resid, rows=None):
     _check(load().nf4o_gemv_residual(_ptr(codes), _ptr(scales), M, K, _ptr(x), _xtype(x), _ptr(resid),
                                      _ptr(r), n, _ptr(y64), _ptr(y32)), "gemv_residual")
     return y64, y32
+
+
+def gemv_qkv(parts, x, rows=None):
+    """Fused q/k/v projection: parts = [(codes, scales, bias or None)] x 3 (q, k,
+    v; same K).  float64 y and magnitude S over the concatenated row space (q
+    rows, then k, then v), for the requested rows (all if None)."""
+    assert len(parts) == 3
+    cs = [np.ascontiguousarray(c, np.uint8) for c, _, _ in parts]
+    ss = [np.ascontiguousarray(s_, np.float32) for _, s_, _ in parts]
+    bs = [None if b is None else np.ascontiguousarray(b, np.float32) for _, _, b in parts]
+    Ms = [c.shape[0] for c in cs]
+    K = cs[0].shape[1] * 2
+    assert all(c.shape[1] * 2 == K for c in cs)
+    x = np.ascontiguousarray(x)
+    r, n = _rows(rows, sum(Ms))
+    V3 = ctypes.c_void_p * 3
+    y = np.zeros(n, np.float64)
+    S = np.zeros(n, np.float64)
+    _check(load().nf4o_gemv_qkv(V3(*[_ptr(c) for c in cs]), V3(*[_ptr(s_) for s_ in ss]),
+                                V3(*[_ptr(b) for b in bs]), (ctypes.c_int64 * 3)(*Ms), K, _ptr(x), _xtype(x),
+                                _ptr(r), n, _ptr(y), _ptr(S)), "gemv_qkv")
+    return y, S
 
 
 def gemv_swiglu(g_codes, g_scales, u_codes, u_scales, x, rows=None):

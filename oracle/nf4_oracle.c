@@ -251,6 +251,40 @@ int nf4o_gemv_residual(const uint8_t* codes, const float* scales, int64_t M, int
   return NF4O_OK;
 }
 
+/*
+ * Fused q/k/v projection ("Decode V2 -- resident executor", section 6: one
+ * grid over q.M + k.M + v.M rows sharing x, the q/k/v bias added in the same
+ * kernel).  The row space is the three matrices' rows in the order q, k, v;
+ * for row r of matrix p:
+ *   y = sum_k W_hat_p[r][k] * x[k] + b_p[r]      (float64, k ascending)
+ *   S = sum_k |W_hat_p[r][k] * x[k]| + |b_p[r]|
+ * b_p NULL means no bias for matrix p.  rows[] index the concatenated row
+ * space (all rows in order when rows is NULL); y or S may be NULL.
+ */
+int nf4o_gemv_qkv(const uint8_t* const codes[3], const float* const scales[3], const float* const bias[3],
+                  const int64_t M[3], int64_t K, const void* x, int xt, const int64_t* rows, int64_t nrows,
+                  double* y, double* S) {
+  if (!codes || !scales || !bias || !M) return NF4O_EINVAL;
+  const int64_t total = M[0] + M[1] + M[2];
+  if (!rows) nrows = total;
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t r = rows ? rows[i] : i;
+    if (r < 0 || r >= total) return NF4O_EINVAL;
+    int p = 0;
+    while (r >= M[p]) {
+      r -= M[p];
+      ++p;
+    }
+    double acc, mag;
+    int st = nf4o_gemv(codes[p], scales[p], M[p], K, x, xt, &r, 1, &acc, &mag);
+    if (st) return st;
+    const double b = bias[p] ? (double)bias[p][r] : 0.0;
+    if (y) y[i] = acc + b;
+    if (S) S[i] = mag + fabs(b);
+  }
+  return NF4O_OK;
+}
+
 /* silu(z) = z / (1 + e^-z), float64 */
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 

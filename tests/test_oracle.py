@@ -6,6 +6,8 @@ Encoder: exact rational brute force, round trip, error bound, zero block.
 GEMV: hand-computed worked examples (tests/golden/worked_examples.txt), exact
 sums via math.fsum, numpy float64 matmul, power-of-two linearity, the zero level.
 Epilogues: residual / SwiGLU / argmax reduce to the GEMV plus their definitions;
+fused q/k/v: a worked example with distinct closed-form values per segment, zero
+scales giving exactly the bias, row sampling across the segment boundaries;
 argmax ties go to the lowest index ("golang.design/x/accel/tensor", func Argmax).
 Chunk: equals the GEMV exactly when every W_hat is representable in bf16, and
 otherwise stays within the bf16 rounding bound of the weights.
@@ -452,3 +454,67 @@ def test_chunk_explicit_bf16_products(oracle_mod, cb):
     for n in range(2):
         for m in range(3):
             assert abs(Y[n, m] - math.fsum(Wb[m] * Xf[n])) <= 1e-14 * np.sum(np.abs(Wb[m] * Xf[n]))
+
+
+# ------------------------------------------------------------- fused q/k/v
+
+
+def _const_codes(M, K, byte):
+    return np.full((M, K // 2), byte, np.uint8)
+
+
+def test_qkv_worked_example(oracle_mod, cb):
+    # q rows: every code 15 (level +1); k rows: code 0 (level -1); v rows: code 7
+    # (level 0).  Scale 0.5 everywhere, x = 1 (K = 128), bias b = row index / 4.
+    # Then y_q = 128 * 0.5 + b = 64 + b, y_k = -64 + b, y_v = b, exactly.
+    assert cb[15] == 1.0 and cb[0] == -1.0 and cb[7] == 0.0
+    K = 128
+    Mq, Mk, Mv = 6, 2, 3
+    parts = []
+    for M, byte in ((Mq, 0xFF), (Mk, 0x00), (Mv, 0x77)):
+        bias = (np.arange(M, dtype=np.float32) / 4).astype(np.float32)
+        parts.append((_const_codes(M, K, byte), np.full((M, K // 64), 0.5, np.float32), bias))
+    y, S = oracle_mod.gemv_qkv(parts, np.ones(K, np.float32))
+    want = [64 + i / 4 for i in range(Mq)] + [-64 + i / 4 for i in range(Mk)] + [i / 4 for i in range(Mv)]
+    assert list(y) == want
+    assert list(S) == [64 + i / 4 for i in range(Mq)] + [64 + i / 4 for i in range(Mk)] + [i / 4 for i in range(Mv)]
+    # no bias on k: k rows become exactly -64
+    parts[1] = (parts[1][0], parts[1][1], None)
+    y2, _ = oracle_mod.gemv_qkv(parts, np.ones(K, np.float32))
+    assert list(y2[Mq:Mq + Mk]) == [-64.0, -64.0]
+    assert np.array_equal(y2[:Mq], y[:Mq]) and np.array_equal(y2[Mq + Mk:], y[Mq + Mk:])
+
+
+def test_qkv_zero_scales_give_the_bias(oracle_mod):
+    K = 256
+    parts = []
+    for t, M in enumerate((5, 3, 4)):
+        codes, _ = oracle_mod.quantize(synth.weights(70 + t, 0, M, K))
+        bias = synth.normal_f32(70 + t, 1, M)
+        parts.append((codes, np.zeros((M, K // 64), np.float32), bias))
+    y, S = oracle_mod.gemv_qkv(parts, synth.normal_bf16(70, 2, K))
+    b = np.concatenate([p[2] for p in parts]).astype(np.float64)
+    assert np.array_equal(y, b) and np.array_equal(S, np.abs(b))
+
+
+def test_qkv_rows_span_segments(oracle_mod):
+    # sampled rows across the q/k and k/v boundaries equal the unsampled ones,
+    # and each segment equals the exact sum of its own dequantized products
+    K = 512
+    parts = []
+    for t, M in enumerate((7, 2, 5)):
+        codes, scales = oracle_mod.quantize(synth.weights(80 + t, 0, M, K))
+        parts.append((codes, scales, synth.normal_f32(80 + t, 1, M)))
+    x = synth.normal_bf16(80, 2, K)
+    y, S = oracle_mod.gemv_qkv(parts, x)
+    rows = [13, 0, 6, 7, 8, 9]
+    ys, Ss = oracle_mod.gemv_qkv(parts, x, rows=rows)
+    assert np.array_equal(ys, y[rows]) and np.array_equal(Ss, S[rows])
+    xf = synth.bf16_to_f32(x).astype(np.float64)
+    base = 0
+    for codes, scales, bias in parts:
+        W_hat = oracle_mod.dequant(codes, scales).astype(np.float64)
+        for m in range(codes.shape[0]):
+            terms = W_hat[m] * xf
+            assert abs(y[base + m] - (math.fsum(terms) + float(bias[m]))) <= 1e-13 * S[base + m]
+        base += codes.shape[0]
