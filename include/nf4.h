@@ -112,6 +112,25 @@ nf4_status nf4_gemv_swiglu(const nf4_weight* Wg, const nf4_weight* Wu, const voi
                            uint16_t* out, nf4_stream stream);
 
 /*
+ * Fused q/k/v projection, one launch over the three matrices' rows sharing x:
+ *   q[m] = sum_k Wq_hat[m][k] * x[k] + bq[m]   (likewise k with Wk, bk and v with Wv, bv)
+ * Source: same page, section 6 ("one grid over q.M+k.M+v.M rows sharing x (no
+ * packed copy)"; the q/k/v bias of Qwen2.5-style models is added in that
+ * kernel, and dropping it changes the greedy ids).  The three weights stay in
+ * their own buffers; the row space is q's rows, then k's, then v's, and a
+ * block's range may span two matrices.
+ *   Wq, Wk, Wv  weights with a common K (any M each; q.M + k.M + v.M < 2^31)
+ *   bq, bk, bv  fp32 biases of length q.M, k.M, v.M, 4-byte aligned, or NULL
+ *               for no bias; added once to the fp32 row sum
+ *   q, k, v     fp32 outputs of length q.M, k.M, v.M (may be consecutive parts
+ *               of one buffer)
+ * Errors: as nf4_gemv, plus NF4_EINVAL when the K differ.
+ */
+nf4_status nf4_gemv_qkv(const nf4_weight* Wq, const nf4_weight* Wk, const nf4_weight* Wv, const float* bq,
+                        const float* bk, const float* bv, const void* x, nf4_dtype xt, float* q, float* k, float* v,
+                        nf4_stream stream);
+
+/*
  * logits[m] = sum_k W_hat[m][k] * x[k];  *index = min{ m : logits[m] = max_j logits[j] }
  * Source: same page, section 5 (final lm_head -> next_token = argmax(logits),
  * the id stays on the device) and "golang.design/x/accel/tensor", func Argmax

@@ -163,9 +163,16 @@ bool use_register_kernel() {
   return v;
 }
 
+// The three matrices of a fused q/k/v call with their biases and outputs.
+struct QkvParts {
+  const nf4_weight* W[3];
+  const float* bias[3];
+  float* out[3];
+};
+
 nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const void* x, nf4_dtype xt,
                     const float* resid, float* y, uint16_t* out, int64_t* index, void* ws, nf4_stream stream,
-                    const char* what) {
+                    const char* what, const QkvParts* qkv = nullptr) {
   int dev = 0;
   nf4_status st = current_device(&dev);
   if (st) return st;
@@ -185,9 +192,23 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
   a.M = (int)W->M;
   a.K = (int)W->K;
   a.cb = codebook();
-  const bool scales16 = aligned(W->scales, 16) && (!W2 || aligned(W2->scales, 16));
+  bool scales16_extra = true;
+  if (qkv) {  // one row space: q's rows, then k's, then v's
+    int64_t end = 0;
+    for (int i = 0; i < 3; ++i) {
+      a.seg_codes[i] = qkv->W[i]->codes;
+      a.seg_scales[i] = qkv->W[i]->scales;
+      a.seg_bias[i] = qkv->bias[i];
+      a.seg_out[i] = qkv->out[i];
+      end += qkv->W[i]->M;
+      a.seg_end[i] = (int)end;
+      scales16_extra = scales16_extra && aligned(qkv->W[i]->scales, 16);
+    }
+    a.M = (int)end;
+  }
+  const bool scales16 = aligned(W->scales, 16) && (!W2 || aligned(W2->scales, 16)) && scales16_extra;
   if (scales16 && !use_register_kernel()) {
-    const nf4k::TmaConfig tc = nf4k::choose_tma_config(epi, xt == NF4_BF16, W->M, W->K, dev);
+    const nf4k::TmaConfig tc = nf4k::choose_tma_config(epi, xt == NF4_BF16, a.M, W->K, dev);
     if (tc.ok) {
       a.G = tc.G;
       a.gpc = tc.gpc;
@@ -198,7 +219,7 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
       return NF4_OK;
     }
   }
-  const nf4k::GemvConfig cfg = nf4k::choose_gemv_config(epi, W->M, W->K, dev);
+  const nf4k::GemvConfig cfg = nf4k::choose_gemv_config(epi, a.M, W->K, dev);
   a.G = cfg.G;
   a.gpc = cfg.gpc;
   const cudaError_t e = nf4k::launch_gemv(epi, xt == NF4_BF16, a, cfg, reinterpret_cast<cudaStream_t>(stream));
@@ -330,6 +351,30 @@ nf4_status nf4_gemv_argmax(const nf4_weight* W, const void* x, nf4_dtype xt, flo
       (st = check_out(index, 8, "index", what)) || (st = check_out(workspace, 8, "workspace", what)))
     return st;
   return run_gemv(nf4k::EPI_ARGMAX, W, nullptr, x, xt, nullptr, logits, nullptr, index, workspace, stream, what);
+}
+
+nf4_status nf4_gemv_qkv(const nf4_weight* Wq, const nf4_weight* Wk, const nf4_weight* Wv, const float* bq,
+                        const float* bk, const float* bv, const void* x, nf4_dtype xt, float* q, float* k, float* v,
+                        nf4_stream stream) {
+  const char* what = "nf4_gemv_qkv";
+  nf4_status st;
+  if ((st = check_weight(Wq, what)) || (st = check_weight(Wk, what)) || (st = check_weight(Wv, what)) ||
+      (st = check_x(x, xt, what)) || (st = check_out(q, 4, "q", what)) || (st = check_out(k, 4, "k", what)) ||
+      (st = check_out(v, 4, "v", what)))
+    return st;
+  if (Wk->K != Wq->K || Wv->K != Wq->K)
+    return fail(NF4_EINVAL, "%s: q, k and v must share K (got %lld, %lld, %lld)", what, (long long)Wq->K,
+                (long long)Wk->K, (long long)Wv->K);
+  if (Wq->M + Wk->M + Wv->M >= ((int64_t)1 << 31))
+    return fail(NF4_EINVAL, "%s: q.M + k.M + v.M = %lld rows exceeds 2^31 - 1", what,
+                (long long)(Wq->M + Wk->M + Wv->M));
+  const float* bias[3] = {bq, bk, bv};
+  const char* bname[3] = {"bq", "bk", "bv"};
+  for (int i = 0; i < 3; ++i)
+    if (bias[i] && !aligned(bias[i], 4)) return fail(NF4_EALIGN, "%s: %s must be 4-byte aligned", what, bname[i]);
+  QkvParts parts{{Wq, Wk, Wv}, {bq, bk, bv}, {q, k, v}};
+  return run_gemv(nf4k::EPI_QKV, Wq, nullptr, x, xt, nullptr, nullptr, nullptr, nullptr, nullptr, stream, what,
+                  &parts);
 }
 
 nf4_status nf4_gemm_chunk(const nf4_weight* W, const uint16_t* X, int N, float* Y, void* workspace,

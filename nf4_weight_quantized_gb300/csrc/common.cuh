@@ -319,7 +319,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 }
 
 // Epilogue kinds of the N=1 kernel.
-enum Epi : int { EPI_PLAIN = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
+enum Epi : int { EPI_PLAIN = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3, EPI_QKV = 4 };
 
 // Arguments of one N=1 launch.
 struct GemvArgs {
@@ -338,7 +338,39 @@ struct GemvArgs {
   int G;    // threads cooperating on one row (multiple of 32)
   int gpc;  // row groups per block
   Codebook cb;
+  // fused q/k/v (EPI_QKV): one row space over three matrices sharing x; rows
+  // [0, seg_end[0]) are matrix 0's, [seg_end[0], seg_end[1]) matrix 1's,
+  // [seg_end[1], seg_end[2]) matrix 2's.  Bias pointers may be null.
+  const uint8_t* seg_codes[3];
+  const float* seg_scales[3];
+  const float* seg_bias[3];
+  float* seg_out[3];
+  int seg_end[3];
 };
+
+// Segment of a row of the fused q/k/v row space, its first row, and its
+// members (selected without indexing the parameter arrays at run time).
+__device__ __forceinline__ int qkv_seg(const GemvArgs& a, int64_t row) {
+  return row < a.seg_end[0] ? 0 : (row < a.seg_end[1] ? 1 : 2);
+}
+__device__ __forceinline__ int64_t qkv_first(const GemvArgs& a, int s) {
+  return s == 0 ? 0 : (s == 1 ? a.seg_end[0] : a.seg_end[1]);
+}
+__device__ __forceinline__ int64_t qkv_end(const GemvArgs& a, int s) {
+  return s == 0 ? a.seg_end[0] : (s == 1 ? a.seg_end[1] : a.seg_end[2]);
+}
+template <typename T>
+__device__ __forceinline__ T qkv_pick(int s, T v0, T v1, T v2) {
+  return s == 0 ? v0 : (s == 1 ? v1 : v2);
+}
+// fused q/k/v epilogue: y = sum + bias, into the segment's own output
+__device__ __forceinline__ void qkv_store(const GemvArgs& a, int64_t row, float v) {
+  const int s = qkv_seg(a, row);
+  const int64_t lr = row - qkv_first(a, s);
+  const float* b = qkv_pick(s, a.seg_bias[0], a.seg_bias[1], a.seg_bias[2]);
+  float* o = qkv_pick(s, a.seg_out[0], a.seg_out[1], a.seg_out[2]);
+  o[lr] = b ? v + b[lr] : v;
+}
 
 // Kernel configuration for an N=1 launch (chosen on the host per shape).
 struct GemvConfig {

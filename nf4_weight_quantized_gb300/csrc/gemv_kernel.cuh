@@ -145,8 +145,17 @@ __device__ __forceinline__ void gemv_body(const GemvArgs& a) {
         for (int j = 0; j < NCH; ++j) {
           const int64_t row = rb0 + i;
           if (row < r1 && cval[j]) {
-            B.c[n][i][j] = ld_stream_v4(codes[n] + row * row_bytes + (int64_t)cidx[j] * 16);
-            B.s[n][i][j] = ld_nc_f32(scales[n] + row * nblk + (cidx[j] >> 1));
+            const uint8_t* cp = codes[n];
+            const float* sp = scales[n];
+            int64_t lr = row;
+            if (EPI == EPI_QKV) {  // the row's own matrix
+              const int sg = qkv_seg(a, row);
+              lr = row - qkv_first(a, sg);
+              cp = qkv_pick(sg, a.seg_codes[0], a.seg_codes[1], a.seg_codes[2]);
+              sp = qkv_pick(sg, a.seg_scales[0], a.seg_scales[1], a.seg_scales[2]);
+            }
+            B.c[n][i][j] = ld_stream_v4(cp + lr * row_bytes + (int64_t)cidx[j] * 16);
+            B.s[n][i][j] = ld_nc_f32(sp + lr * nblk + (cidx[j] >> 1));
           } else {
             B.c[n][i][j] = make_uint4(0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);
             B.s[n][i][j] = 0.f;
@@ -254,6 +263,8 @@ __device__ __forceinline__ void gemv_body(const GemvArgs& a) {
         const float u = v[NV - 1];
         const float silu = g / (1.0f + expf(-g));
         a.out_bf16[row] = __bfloat16_as_ushort(__float2bfloat16_rn(silu * u));
+      } else if (EPI == EPI_QKV) {
+        qkv_store(a, row, v[0]);
       } else {
         a.y[row] = v[0];
         const unsigned long long k = argmax_key(v[0], row);

@@ -157,6 +157,26 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     mcodes[NV - 1] = a.codes2;
     mscales[NV - 1] = a.scales2;
   }
+  // Rows [g, g + n) of the row space as contiguous pieces of one matrix each:
+  // fn(codes, scales, first row in that matrix, first stage row, rows).  Only
+  // the fused q/k/v row space has more than one piece (segment boundaries).
+  auto for_pieces = [&](int n_mat, int64_t g, int n, int srow, auto&& fn) {
+    if (EPI != EPI_QKV) {
+      fn(mcodes[n_mat], mscales[n_mat], g, srow, n);
+      return;
+    }
+    while (n > 0) {
+      const int sg = qkv_seg(a, g);
+      const int64_t first = qkv_first(a, sg);
+      const int64_t end = qkv_end(a, sg);
+      const int piece = (int)((end - g) < n ? (end - g) : n);
+      fn(qkv_pick(sg, a.seg_codes[0], a.seg_codes[1], a.seg_codes[2]),
+         qkv_pick(sg, a.seg_scales[0], a.seg_scales[1], a.seg_scales[2]), g - first, srow, piece);
+      g += piece;
+      srow += piece;
+      n -= piece;
+    }
+  };
   // one stage: per full barrier, the codes and scales of its SUBR rows (rows
   // are contiguous in memory and in the stage, so one copy per matrix each);
   // a barrier whose rows lie past the block's end is completed by a plain
@@ -178,12 +198,13 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
       const uint32_t sb = (uint32_t)nr * (uint32_t)nblk * 4u;
       mbar_arrive_expect_tx(fb, NV * (cb + sb));
 #pragma unroll
-      for (int n = 0; n < NV; ++n) {
-        bulk_g2s(smem_addr(st + n * P.codes_bytes + r0 * row_bytes), mcodes[n] + (rb + r0) * row_bytes, cb, fb,
-                 policy);
-        bulk_g2s(smem_addr(st + NV * P.codes_bytes + n * P.scales_bytes + r0 * nblk * 4),
-                 mscales[n] + (rb + r0) * nblk, sb, fb, policy);
-      }
+      for (int n = 0; n < NV; ++n)
+        for_pieces(n, rb + r0, nr, r0, [&](const uint8_t* cp, const float* sp, int64_t lr, int sr, int pr) {
+          bulk_g2s(smem_addr(st + n * P.codes_bytes + sr * row_bytes), cp + lr * row_bytes,
+                   (uint32_t)pr * (uint32_t)row_bytes, fb, policy);
+          bulk_g2s(smem_addr(st + NV * P.codes_bytes + n * P.scales_bytes + sr * nblk * 4), sp + lr * nblk,
+                   (uint32_t)pr * (uint32_t)nblk * 4u, fb, policy);
+        });
     }
   };
   // Before the previous kernel on the stream has finished (programmatic
@@ -196,10 +217,11 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
       const int64_t rb = R0 + (int64_t)it * P.SR;
       const int rows = (int)((R1 - rb) < P.SR ? (R1 - rb) : P.SR);
 #pragma unroll
-      for (int n = 0; n < NV; ++n) {
-        bulk_prefetch_l2(mcodes[n] + rb * row_bytes, (uint32_t)rows * (uint32_t)row_bytes);
-        bulk_prefetch_l2(mscales[n] + rb * nblk, (uint32_t)rows * (uint32_t)nblk * 4u);
-      }
+      for (int n = 0; n < NV; ++n)
+        for_pieces(n, rb, rows, 0, [&](const uint8_t* cp, const float* sp, int64_t lr, int, int pr) {
+          bulk_prefetch_l2(cp + lr * row_bytes, (uint32_t)pr * (uint32_t)row_bytes);
+          bulk_prefetch_l2(sp + lr * nblk, (uint32_t)pr * (uint32_t)nblk * 4u);
+        });
     }
   }
 
@@ -437,6 +459,8 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
           const float u = v[NV - 1];
           const float silu = g / (1.0f + expf(-g));
           a.out_bf16[row] = __bfloat16_as_ushort(__float2bfloat16_rn(silu * u));
+        } else if (EPI == EPI_QKV) {
+          qkv_store(a, row, v[0]);
         } else {
           a.y[row] = v[0];
           const unsigned long long k = argmax_key(v[0], row);

@@ -52,6 +52,7 @@ def _load():
         "nf4_gemv": [W, P, I, P, P],
         "nf4_gemv_residual": [W, P, I, P, P, P],
         "nf4_gemv_swiglu": [W, W, P, I, P, P],
+        "nf4_gemv_qkv": [W, W, W, P, P, P, P, I, P, P, P, P],
         "nf4_gemv_argmax": [W, P, I, P, P, P, P],
         "nf4_gemm_chunk": [W, P, I, P, P, P],
         "nf4_gemm_chunk_noalloc": [W, P, I, P, P],
@@ -78,7 +79,7 @@ lib = _load()
 
 EXPORTS = ("nf4_gemv", "nf4_gemv_residual", "nf4_gemv_swiglu", "nf4_gemv_argmax", "nf4_gemm_chunk",
            "nf4_workspace_bytes", "nf4_quantize", "nf4_codebook", "nf4_last_error", "nf4_describe_config",
-           "nf4_check_device_errors", "nf4_gemm_chunk_noalloc")
+           "nf4_check_device_errors", "nf4_gemm_chunk_noalloc", "nf4_gemv_qkv")
 
 
 def _check(status: int):
@@ -173,6 +174,24 @@ def nf4_gemv_swiglu(Wg: NF4Weight, Wu: NF4Weight, x: torch.Tensor, out: torch.Te
     _check(lib.nf4_gemv_swiglu(ctypes.byref(g), ctypes.byref(u), _dev(x, "x", numel=Wg.K), _xtype(x),
                                _dev(out, "out", torch.bfloat16, Wg.M), _stream(stream)))
     return out
+
+
+def nf4_gemv_qkv(Wq: NF4Weight, Wk: NF4Weight, Wv: NF4Weight, x: torch.Tensor, bq: torch.Tensor | None = None,
+                 bk: torch.Tensor | None = None, bv: torch.Tensor | None = None, q: torch.Tensor | None = None,
+                 k: torch.Tensor | None = None, v: torch.Tensor | None = None, stream=None):
+    """One launch over the q, k and v rows sharing x, each bias (fp32, or None)
+    added to its own rows.  Returns (q, k, v), fp32."""
+    outs = []
+    for o, W in ((q, Wq), (k, Wk), (v, Wv)):
+        outs.append(torch.empty(W.M, dtype=torch.float32, device=x.device) if o is None else o)
+    ws = [Wq.struct(), Wk.struct(), Wv.struct()]
+    bias = [None if b is None else _dev(b, name, torch.float32, W.M)
+            for b, name, W in ((bq, "bq", Wq), (bk, "bk", Wk), (bv, "bv", Wv))]
+    _check(lib.nf4_gemv_qkv(ctypes.byref(ws[0]), ctypes.byref(ws[1]), ctypes.byref(ws[2]), *bias,
+                            _dev(x, "x", numel=Wq.K), _xtype(x),
+                            *[_dev(o, n, torch.float32, W.M) for o, n, W in zip(outs, "qkv", (Wq, Wk, Wv))],
+                            _stream(stream)))
+    return tuple(outs)
 
 
 def nf4_workspace_bytes(M: int, K: int, N: int = 1) -> int:

@@ -326,3 +326,78 @@ def test_errors_are_raised(nf4):
     with pytest.raises(nf4.NF4Error) as e:
         nf4.nf4_gemv(bad, torch.zeros(96, device="cuda"))
     assert e.value.status == -1
+
+
+# ------------------------------------------------------------- fused q/k/v
+
+
+def _qkv_case(nf4, Ms, K, xd, bias_mask, seed, one_buffer=False):
+    parts, Wt, bt = [], [], []
+    for t, M in enumerate(Ms):
+        codes, scales = H.quantized(seed, t, M, K)
+        b = synth.normal_f32(seed, 10 + t, M) if bias_mask[t] else None
+        parts.append((codes, scales, b))
+        Wt.append(H.weight_tensors(codes, scales))
+        bt.append(None if b is None else torch.from_numpy(b).cuda())
+    x = H.make_x(seed, K, xd)
+    y64, S = oracle.gemv_qkv(parts, x)
+    if one_buffer:  # q, k, v as consecutive parts of one output buffer
+        buf = torch.full((sum(Ms) + 8,), 777.0, device="cuda")
+        outs = (buf[:Ms[0]], buf[Ms[0]:Ms[0] + Ms[1]], buf[Ms[0] + Ms[1]:sum(Ms)])
+        nf4.nf4_gemv_qkv(*Wt, H.x_tensor(x), *bt, *outs)
+        got = buf.cpu().numpy()
+        assert np.all(got[sum(Ms):] == 777.0), "wrote past v"
+        got = got[:sum(Ms)]
+    else:
+        q, k, v = nf4.nf4_gemv_qkv(*Wt, H.x_tensor(x), *bt)
+        got = np.concatenate([q.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy()])
+    H.assert_within(got, y64, S, extra=H.ulp_f32(y64), what=f"qkv {Ms}x{K} {xd}")
+    return got
+
+
+@pytest.mark.parametrize("Ms,K", [((2048, 256, 256), 2048), ((5120, 1024, 1024), 5120), ((300, 70, 130), 512),
+                                  ((1, 1, 1), 256), ((129, 3, 500), 11008)])
+@pytest.mark.parametrize("xd", ["f32", "bf16"])
+def test_qkv_shapes(nf4, Ms, K, xd):
+    # bulk-copy kernel (K % 256 == 0): block row ranges span the q/k and k/v boundaries
+    _qkv_case(nf4, Ms, K, xd, (True, True, True), 700 + sum(Ms) % 97)
+
+
+@pytest.mark.parametrize("Ms,K", [((300, 70, 130), 320), ((896, 128, 128), 896)])
+def test_qkv_register_kernel(nf4, Ms, K):
+    # K % 256 != 0: the register-prefetch kernel with the same segment mapping
+    _qkv_case(nf4, Ms, K, "bf16", (True, False, True), 710 + K)
+
+
+def test_qkv_bias_optional_and_one_output_buffer(nf4):
+    Ms, K = (640, 128, 128), 1024
+    with_b = _qkv_case(nf4, Ms, K, "bf16", (True, True, True), 720, one_buffer=True)
+    no_b = _qkv_case(nf4, Ms, K, "bf16", (False, True, False), 720, one_buffer=True)
+    # q rows: biased in one call only, so they differ; k rows: biased in both, identical
+    assert not np.array_equal(with_b[:Ms[0]], no_b[:Ms[0]])
+    assert np.array_equal(with_b[Ms[0]:Ms[0] + Ms[1]], no_b[Ms[0]:Ms[0] + Ms[1]])
+
+
+def test_qkv_equals_separate_projections(nf4):
+    # no bias: each segment agrees with the plain GEMV of its own matrix (both
+    # within the kernel bound of the same float64 sum)
+    Ms, K = (2048, 256, 256), 2048
+    got = _qkv_case(nf4, Ms, K, "bf16", (False, False, False), 730)
+    base = 0
+    for t, M in enumerate(Ms):
+        codes, scales = H.quantized(730, t, M, K)
+        x = H.make_x(730, K, "bf16")
+        y = nf4.nf4_gemv(H.weight_tensors(codes, scales), H.x_tensor(x)).cpu().numpy()
+        _, S = oracle.gemv(codes, scales, x)
+        assert np.all(np.abs(got[base:base + M] - y) <= 2 * KERNEL_REL * S)
+        base += M
+
+
+def test_qkv_errors(nf4):
+    codes, scales = H.quantized(740, 0, 64, 512)
+    W = H.weight_tensors(codes, scales)
+    codes2, scales2 = H.quantized(740, 1, 64, 256)
+    W2 = H.weight_tensors(codes2, scales2)
+    x = H.x_tensor(H.make_x(740, 512, "bf16"))
+    with pytest.raises(nf4.NF4Error, match="share K"):
+        nf4.nf4_gemv_qkv(W, W2, W, x)
