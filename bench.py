@@ -18,7 +18,7 @@ back inside the timed region (weights stay resident, as in decode).
 ``--impl reference`` times the CPU oracle instead (the reference arm of this
 repository; it is deliberately slow, plain C, single-threaded).
 
-Other workloads (SwiGLU, lm_head + argmax, 14B N=1, 14B chunk) are reported
+Other workloads (SwiGLU, lm_head + argmax, 14B N=1, 14B chunk, fused 3B q/k/v) are reported
 under "workloads" with the same method and fewer calls.
 """
 from __future__ import annotations
@@ -123,10 +123,14 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workloads
 
-def bytes_of(kind: str, M: int, K: int, N: int = 1) -> dict:
+def bytes_of(kind: str, M: int, K: int, N: int = 1, M_kv: int = 0) -> dict:
     """Algorithmic bytes per call: weight (codes + scales) and total."""
+    if kind == "qkv":
+        M = M + 2 * M_kv
     w = M * K // 2 + M * (K // 64) * 4
-    if kind == "residual":
+    if kind == "qkv":
+        tot = w + K * 2 + M * 4 + M * 4  # + biases + outputs
+    elif kind == "residual":
         tot = w + K * 2 + M * 4 + M * 4
     elif kind == "swiglu":
         w *= 2
@@ -148,7 +152,7 @@ def build_calls(name: str, torch, nf4, synth, device, copies=None):
     M, K = w.M, w.K
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 128 << 20)
-    b = bytes_of(w.kind, M, K, w.N)
+    b = bytes_of(w.kind, M, K, w.N, w.M_kv)
     fixed_copies = copies
     copies = copies or max(2, int(np.ceil(3 * l2 / b["weight"])))
     d = synth.workload_inputs(w)
@@ -191,6 +195,15 @@ def build_calls(name: str, torch, nf4, synth, device, copies=None):
         ws = nf4.new_workspace(M, K, 1, device)
         call = lambda i, s: nf4.nf4_gemv_argmax(Ws[i % copies], x, logits, index, ws, stream=s)
         ctx = {"W": Ws, "x": x, "logits": logits, "index": index}
+    elif w.kind == "qkv":
+        Wq, Wk, Wv = replicate(quant(d["W"])), replicate(quant(d["Wk"])), replicate(quant(d["Wv"]))
+        x = bf16(d["x"])
+        bq, bk, bv = (torch.from_numpy(d[k]).to(device) for k in ("bq", "bk", "bv"))
+        out = torch.empty(M + 2 * w.M_kv, device=device)
+        qo, ko, vo = out[:M], out[M:M + w.M_kv], out[M + w.M_kv:]
+        call = lambda i, s: nf4.nf4_gemv_qkv(Wq[i % copies], Wk[i % copies], Wv[i % copies], x, bq, bk, bv,
+                                             qo, ko, vo, stream=s)
+        ctx = {"W": (Wq, Wk, Wv), "x": x, "b": (bq, bk, bv), "out": out}
     elif w.kind == "chunk":
         Ws = replicate(quant(d["W"]))
         X = bf16(d["X"])
@@ -387,7 +400,7 @@ def run_gpu(args, rank, world, dist):
 
     workloads = {}
     if args.all_workloads:
-        for name in ("swiglu", "lm_head_argmax", "gemv14b", "chunk14b"):
+        for name in ("swiglu", "lm_head_argmax", "gemv14b", "chunk14b", "qkv3b"):
             try:
                 c2, cp2, b2, ctx2 = build_calls(name, torch, nf4, synth, device)
                 n2 = args.workload_steps
@@ -398,7 +411,8 @@ def run_gpu(args, rank, world, dist):
                     "algorithmic_gbs": b2["total"] / pc / 1e9,
                     "frac_of_hbm": b2["total"] / pc / 1e9 / peaks["hbm_gbs"],
                     "algorithmic_bytes": b2["total"], "traffic": ncu_traffic(name), "copies": cp2, "calls": n2,
-                    "config": nf4.nf4_describe_config(synth.WORKLOADS[name].M, synth.WORKLOADS[name].K,
+                    "config": nf4.nf4_describe_config(synth.WORKLOADS[name].M + 2 * synth.WORKLOADS[name].M_kv,
+                                                      synth.WORKLOADS[name].K,
                                                       synth.WORKLOADS[name].N)}
                 del ctx2, c2
                 torch.cuda.empty_cache()
@@ -446,7 +460,7 @@ def run_profile_target(name: str, calls: int):
     torch.cuda.synchronize()
     w = synth.WORKLOADS[name]
     print(json.dumps({"workload": name, "calls": calls, "algorithmic_bytes": b["total"],
-                      "config": nf4.nf4_describe_config(w.M, w.K, w.N)}))
+                      "config": nf4.nf4_describe_config(w.M + 2 * w.M_kv, w.K, w.N)}))
 
 
 def main():

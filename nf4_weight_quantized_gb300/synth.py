@@ -48,6 +48,11 @@ def normal_f32(seed: int, tensor_id: int, n: int, std: float = 1.0) -> np.ndarra
     return (std * z).astype(np.float32)
 
 
+def token_ids(seed: int, tensor_id: int, n: int, vocab: int) -> np.ndarray:
+    """n token ids drawn uniformly from [0, vocab), int64."""
+    return rng(seed, tensor_id).integers(0, vocab, n, dtype=np.int64)
+
+
 def weights(seed: int, tensor_id: int, M: int, K: int, std: float = W_STD,
             rows_per_draw: int = 4096) -> np.ndarray:
     """fp32 [M, K] weights ~ N(0, std^2), drawn in row blocks from one stream."""
@@ -78,13 +83,14 @@ def silu_product_bf16(seed: int, tid_a: int, tid_b: int, n: int) -> np.ndarray:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "gemv", "residual", "swiglu", "argmax", "chunk"
+    kind: str  # "gemv", "residual", "swiglu", "argmax", "chunk", "qkv"
     M: int
     K: int
     N: int
     seed: int
     x_dtype: str  # "f32" or "bf16"
     description: str
+    M_kv: int = 0  # qkv: rows of k and of v (M is q's rows)
 
 
 WORKLOADS = {
@@ -100,6 +106,9 @@ WORKLOADS = {
                          "14B-shaped 13824x5120, X 32x5120 bf16 N(0,1), Y fp32 [32][13824]"),
     "gemv14b": Workload("gemv14b", "gemv", 13824, 5120, 1, 4, "bf16",
                         "14B-shaped 13824x5120 at N=1, x = X[0] of the chunk workload"),
+    "qkv3b": Workload("qkv3b", "qkv", 2048, 2048, 1, 5, "bf16",
+                      "3B q/k/v 2048x2048 + 2x 256x2048 in one launch, x bf16 N(0,1), fp32 biases N(0,1)",
+                      M_kv=256),
 }
 
 
@@ -113,7 +122,15 @@ def workload_inputs(w: Workload, M: int | None = None) -> dict:
     K = w.K
     s = w.seed
     d = {}
-    if w.kind == "swiglu":
+    if w.kind == "qkv":
+        d["W"] = weights(s, 0, M, K)
+        d["Wk"] = weights(s, 1, w.M_kv, K)
+        d["Wv"] = weights(s, 2, w.M_kv, K)
+        d["x"] = normal_bf16(s, 3, K)
+        d["bq"] = normal_f32(s, 4, M)
+        d["bk"] = normal_f32(s, 5, w.M_kv)
+        d["bv"] = normal_f32(s, 6, w.M_kv)
+    elif w.kind == "swiglu":
         d["W"] = weights(s, 0, M, K)
         d["Wu"] = weights(s, 1, M, K)
         d["x"] = normal_bf16(s, 2, K)

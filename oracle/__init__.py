@@ -46,6 +46,7 @@ def load():
     lib.nf4o_gemv_argmax.argtypes = [P, P, I64, I64, P, I, P, P, P]
     lib.nf4o_gemm_chunk.argtypes = [P, P, I64, I64, P, I64, P, I64, P, P]
     lib.nf4o_gemv_qkv.argtypes = [P, P, P, P, I64, P, I, P, I64, P, P]
+    lib.nf4o_dequant_rows.argtypes = [P, P, I64, I64, P, I64, P, P, P]
     lib.nf4o_round_bf16.argtypes = [ctypes.c_double]
     lib.nf4o_round_bf16.restype = ctypes.c_uint16
     for name in ("nf4o_codebook", "nf4o_quantize", "nf4o_dequant", "nf4o_gemv", "nf4o_gemv_residual",
@@ -152,6 +153,22 @@ def gemv_qkv(parts, x, rows=None):
                                 V3(*[_ptr(b) for b in bs]), (ctypes.c_int64 * 3)(*Ms), K, _ptr(x), _xtype(x),
                                 _ptr(r), n, _ptr(y), _ptr(S)), "gemv_qkv")
     return y, S
+
+
+def dequant_rows(codes, scales, ids):
+    """Gathered, dequantized rows of an NF4 table: (fp32 [n, K], bf16 bits
+    [n, K], number of ids outside the table, whose rows are zero)."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    ids = np.ascontiguousarray(ids, np.int64)
+    V, K = codes.shape[0], codes.shape[1] * 2
+    n = ids.shape[0]
+    f32 = np.zeros((n, K), np.float32)
+    b16 = np.zeros((n, K), np.uint16)
+    bad = np.zeros(1, np.int64)
+    _check(load().nf4o_dequant_rows(_ptr(codes), _ptr(scales), V, K, _ptr(ids) if n else None, n, _ptr(f32),
+                                    _ptr(b16), _ptr(bad)), "dequant_rows")
+    return f32, b16, int(bad[0])
 
 
 def gemv_swiglu(g_codes, g_scales, u_codes, u_scales, x, rows=None):

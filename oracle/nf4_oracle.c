@@ -285,6 +285,35 @@ int nf4o_gemv_qkv(const uint8_t* const codes[3], const float* const scales[3], c
   return NF4O_OK;
 }
 
+/*
+ * Embedding rows kept as NF4 ("Decode V2 -- resident executor", section 10:
+ * the embedding stays as NF4 rows, gathered and dequantized into the arena,
+ * with no dense [vocab, hidden] table).  For i < n:
+ *   out_f32[i][k]  = W_hat[ids[i]][k]   (level x scale, one fp32 rounding)
+ *   out_bf16[i][k] = that value rounded to bf16 (nearest even)
+ * Rows whose id lies outside [0, V) are written as zeros and counted in *bad.
+ * Any output may be NULL.
+ */
+int nf4o_dequant_rows(const uint8_t* codes, const float* scales, int64_t V, int64_t K, const int64_t* ids,
+                      int64_t n, float* out_f32, uint16_t* out_bf16, int64_t* bad) {
+  if (!shape_ok(V, K) || !codes || !scales || (n > 0 && !ids) || n < 0) return NF4O_EINVAL;
+  float cb[16];
+  nf4o_codebook(cb);
+  int64_t nbad = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t m = ids[i];
+    const int ok = m >= 0 && m < V;
+    nbad += !ok;
+    for (int64_t k = 0; k < K; ++k) {
+      const float w = ok ? what_at(cb, codes, scales, K, m, k) : 0.0f;
+      if (out_f32) out_f32[i * K + k] = w;
+      if (out_bf16) out_bf16[i * K + k] = f64_to_bf16_bits((double)w);
+    }
+  }
+  if (bad) *bad = nbad;
+  return NF4O_OK;
+}
+
 /* silu(z) = z / (1 + e^-z), float64 */
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 

@@ -8,6 +8,8 @@ sums via math.fsum, numpy float64 matmul, power-of-two linearity, the zero level
 Epilogues: residual / SwiGLU / argmax reduce to the GEMV plus their definitions;
 fused q/k/v: a worked example with distinct closed-form values per segment, zero
 scales giving exactly the bias, row sampling across the segment boundaries;
+embedding rows: a worked example with exact values and bf16 bits, out-of-range
+ids giving zero rows, bf16 equal to round-to-nearest-even on the bit pattern;
 argmax ties go to the lowest index ("golang.design/x/accel/tensor", func Argmax).
 Chunk: equals the GEMV exactly when every W_hat is representable in bf16, and
 otherwise stays within the bf16 rounding bound of the weights.
@@ -518,3 +520,43 @@ def test_qkv_rows_span_segments(oracle_mod):
             terms = W_hat[m] * xf
             assert abs(y[base + m] - (math.fsum(terms) + float(bias[m]))) <= 1e-13 * S[base + m]
         base += codes.shape[0]
+
+
+# ------------------------------------------------------- NF4 embedding rows
+
+
+def test_dequant_rows_worked_example(oracle_mod, cb):
+    # row 0: bytes 0xF0 (low nibble 0 -> -1, high nibble 15 -> +1), scale 2.5;
+    # row 1: bytes 0x77 (level 0); row 2: bytes 0x0F (+1, -1), scale -0.5
+    K = 64
+    codes = np.stack([np.full(K // 2, 0xF0, np.uint8), np.full(K // 2, 0x77, np.uint8),
+                      np.full(K // 2, 0x0F, np.uint8)])
+    scales = np.array([[2.5], [7.0], [-0.5]], np.float32)
+    f32, b16, bad = oracle_mod.dequant_rows(codes, scales, np.array([2, 0, 1, 0]))
+    assert bad == 0
+    assert list(f32[1][:4]) == [-2.5, 2.5, -2.5, 2.5] and np.array_equal(f32[1], f32[3])
+    assert list(f32[0][:4]) == [-0.5, 0.5, -0.5, 0.5]
+    assert np.all(f32[2] == 0.0)
+    assert list(b16[1][:2]) == [0xC020, 0x4020]  # -2.5, 2.5 in bf16
+    assert list(b16[0][:2]) == [0xBF00, 0x3F00]  # -0.5, 0.5
+
+
+def test_dequant_rows_out_of_range_ids_are_zero(oracle_mod):
+    codes, scales = oracle_mod.quantize(synth.weights(90, 0, 5, 128))
+    f32, b16, bad = oracle_mod.dequant_rows(codes, scales, np.array([-1, 5, 4, 1 << 40]))
+    assert bad == 3
+    assert np.all(f32[[0, 1, 3]] == 0) and np.all(b16[[0, 1, 3]] == 0)
+    assert np.array_equal(f32[2], oracle_mod.dequant(codes, scales)[4])
+
+
+def test_dequant_rows_bf16_is_round_to_nearest_even(oracle_mod):
+    codes, scales = oracle_mod.quantize(synth.weights(91, 0, 64, 512))
+    ids = synth.token_ids(91, 1, 40, 64)
+    f32, b16, bad = oracle_mod.dequant_rows(codes, scales, ids)
+    assert bad == 0
+    full = oracle_mod.dequant(codes, scales)
+    assert np.array_equal(f32, full[ids])
+    # bf16 rounding written out on the bit pattern (finite values)
+    u = f32.view(np.uint32).astype(np.uint64)
+    rne = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    assert np.array_equal(b16, rne)
