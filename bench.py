@@ -18,7 +18,8 @@ back inside the timed region (weights stay resident, as in decode).
 ``--impl reference`` times the CPU oracle instead (the reference arm of this
 repository; it is deliberately slow, plain C, single-threaded).
 
-Other workloads (SwiGLU, lm_head + argmax, 14B N=1, 14B chunk, fused 3B q/k/v) are reported
+Other workloads (SwiGLU, lm_head + argmax, 14B N=1, 14B chunk, fused 3B q/k/v, embedding-row
+gather of a 4096-token prompt) are reported
 under "workloads" with the same method and fewer calls.
 """
 from __future__ import annotations
@@ -125,6 +126,9 @@ class ClockSampler:
 
 def bytes_of(kind: str, M: int, K: int, N: int = 1, M_kv: int = 0) -> dict:
     """Algorithmic bytes per call: weight (codes + scales) and total."""
+    if kind == "embed":  # N gathered rows of an M-row table: read N rows, write N bf16 rows
+        w = N * (K // 2 + (K // 64) * 4)
+        return {"weight": w, "total": w + N * 8 + N * K * 2, "table": M * K // 2 + M * (K // 64) * 4}
     if kind == "qkv":
         M = M + 2 * M_kv
     w = M * K // 2 + M * (K // 64) * 4
@@ -144,6 +148,14 @@ def bytes_of(kind: str, M: int, K: int, N: int = 1, M_kv: int = 0) -> dict:
     return {"weight": w, "total": tot}
 
 
+def describe(nf4, w) -> str:
+    """The library's description of the launch a workload makes."""
+    if w.kind == "embed":
+        return (f"nf4_dequant_rows: {w.N} rows of a {w.M}x{w.K} NF4 table, bf16 out, one thread per 32 weights, "
+                "256-thread blocks")
+    return nf4.nf4_describe_config(w.M + 2 * w.M_kv, w.K, w.N)
+
+
 def build_calls(name: str, torch, nf4, synth, device, copies=None):
     """Inputs for one workload, quantized on the device, with enough rotating
     weight copies to exceed 3x L2 (or `copies`).  Returns (call(i), n_copies,
@@ -154,7 +166,7 @@ def build_calls(name: str, torch, nf4, synth, device, copies=None):
     l2 = getattr(props, "L2_cache_size", 128 << 20)
     b = bytes_of(w.kind, M, K, w.N, w.M_kv)
     fixed_copies = copies
-    copies = copies or max(2, int(np.ceil(3 * l2 / b["weight"])))
+    copies = copies or max(2, int(np.ceil(3 * l2 / b.get("table", b["weight"]))))
     d = synth.workload_inputs(w)
 
     def quant(Wnp):
@@ -195,6 +207,12 @@ def build_calls(name: str, torch, nf4, synth, device, copies=None):
         ws = nf4.new_workspace(M, K, 1, device)
         call = lambda i, s: nf4.nf4_gemv_argmax(Ws[i % copies], x, logits, index, ws, stream=s)
         ctx = {"W": Ws, "x": x, "logits": logits, "index": index}
+    elif w.kind == "embed":
+        Es = replicate(quant(d["W"]))
+        ids = torch.from_numpy(d["ids"]).to(device)
+        out = torch.empty((w.N, K), dtype=torch.bfloat16, device=device)
+        call = lambda i, s: nf4.nf4_dequant_rows(Es[i % copies], ids, out, stream=s)
+        ctx = {"E": Es, "ids": ids, "out": out}
     elif w.kind == "qkv":
         Wq, Wk, Wv = replicate(quant(d["W"])), replicate(quant(d["Wk"])), replicate(quant(d["Wv"]))
         x = bf16(d["x"])
@@ -400,7 +418,7 @@ def run_gpu(args, rank, world, dist):
 
     workloads = {}
     if args.all_workloads:
-        for name in ("swiglu", "lm_head_argmax", "gemv14b", "chunk14b", "qkv3b"):
+        for name in ("swiglu", "lm_head_argmax", "gemv14b", "chunk14b", "qkv3b", "embed_prefill"):
             try:
                 c2, cp2, b2, ctx2 = build_calls(name, torch, nf4, synth, device)
                 n2 = args.workload_steps
@@ -411,9 +429,7 @@ def run_gpu(args, rank, world, dist):
                     "algorithmic_gbs": b2["total"] / pc / 1e9,
                     "frac_of_hbm": b2["total"] / pc / 1e9 / peaks["hbm_gbs"],
                     "algorithmic_bytes": b2["total"], "traffic": ncu_traffic(name), "copies": cp2, "calls": n2,
-                    "config": nf4.nf4_describe_config(synth.WORKLOADS[name].M + 2 * synth.WORKLOADS[name].M_kv,
-                                                      synth.WORKLOADS[name].K,
-                                                      synth.WORKLOADS[name].N)}
+                    "config": describe(nf4, synth.WORKLOADS[name])}
                 del ctx2, c2
                 torch.cuda.empty_cache()
             except Exception as e:  # report, keep the main line
@@ -460,7 +476,7 @@ def run_profile_target(name: str, calls: int):
     torch.cuda.synchronize()
     w = synth.WORKLOADS[name]
     print(json.dumps({"workload": name, "calls": calls, "algorithmic_bytes": b["total"],
-                      "config": nf4.nf4_describe_config(w.M + 2 * w.M_kv, w.K, w.N)}))
+                      "config": describe(nf4, w)}))
 
 
 def main():

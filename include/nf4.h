@@ -73,7 +73,8 @@ typedef enum nf4_status {
   NF4_ENULL = -3,  /* a required pointer is NULL */
   NF4_ECUDA = -4,  /* a CUDA runtime call or launch failed; see nf4_last_error() */
   NF4_EARCH = -5,  /* the current device is not compute capability 10.3 (sm_103a) */
-  NF4_ETIMEOUT = -6 /* a kernel's bounded wait ran out (nf4_check_device_errors only) */
+  NF4_ETIMEOUT = -6, /* a kernel's bounded wait ran out (nf4_check_device_errors only) */
+  NF4_ERANGE = -7    /* a token id was outside its table (nf4_check_device_errors only) */
 } nf4_status;
 
 /* Activation element type. */
@@ -200,13 +201,30 @@ nf4_status nf4_quantize(const float* W, int64_t M, int64_t K, uint8_t* codes, fl
                         nf4_stream stream);
 
 /*
+ * Embedding rows kept as NF4, gathered and dequantized:
+ *   out[i][k] = W_hat[ids[i]][k] = level(code) * scale   (one fp32 product)
+ * Source: same page, section 10 (the embedding stays as NF4 rows and the rows
+ * a step needs are dequantized into the arena; there is no dense [vocab,
+ * hidden] table).
+ *   E     the [V][K] NF4 table
+ *   ids   [n] int64 token ids on the device, 8-byte aligned; n = 0 does nothing
+ *   out   [n][K] on the device, 16-byte aligned: fp32 (ot = NF4_F32, exact
+ *         products) or bf16 bits (ot = NF4_BF16, rounded to nearest even)
+ * An id outside [0, V) cannot fault: its row is written as zeros and the
+ * next nf4_check_device_errors() returns NF4_ERANGE.
+ */
+nf4_status nf4_dequant_rows(const nf4_weight* E, const int64_t* ids, int64_t n, void* out, nf4_dtype ot,
+                            nf4_stream stream);
+
+/*
  * Diagnostic, not for the hot path: synchronizes the current device, then
  * reads and clears the library's device-side error words.  Kernels that wait
  * on shared-memory barriers (bulk-copy pipelines, tensor-core commits) bound
  * every wait; a wait that runs out (which needs a broken device or library)
  * makes the block skip its remaining work and sets an error word instead of
  * hanging.  Returns NF4_ETIMEOUT if that happened since the last check (the
- * outputs of the calls in between are invalid), NF4_OK otherwise.
+ * outputs of the calls in between are invalid), NF4_ERANGE if nf4_dequant_rows
+ * met an id outside its table, NF4_OK otherwise.
  */
 nf4_status nf4_check_device_errors(void);
 

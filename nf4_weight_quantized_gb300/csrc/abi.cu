@@ -309,7 +309,25 @@ nf4_status nf4_check_device_errors(void) {
   }
   if (bits & nf4k::kErrWaitTimeout)
     return fail(NF4_ETIMEOUT, "a kernel gave up waiting on a shared-memory barrier; its outputs are invalid");
+  if (bits & nf4k::kErrBadIndex)
+    return fail(NF4_ERANGE, "nf4_dequant_rows was given a token id outside its table; those rows were written as zeros");
   return NF4_OK;
+}
+
+nf4_status nf4_dequant_rows(const nf4_weight* E, const int64_t* ids, int64_t n, void* out, nf4_dtype ot,
+                            nf4_stream stream) {
+  const char* what = "nf4_dequant_rows";
+  nf4_status st;
+  if ((st = check_weight(E, what))) return st;
+  if (n < 0) return fail(NF4_EINVAL, "%s: n = %lld is negative", what, (long long)n);
+  if (ot != NF4_F32 && ot != NF4_BF16) return fail(NF4_EINVAL, "%s: output dtype %d is not NF4_F32 or NF4_BF16", what, (int)ot);
+  if (n == 0) return NF4_OK;
+  if ((st = check_out(ids, 8, "ids", what)) || (st = check_out(out, 16, "out", what))) return st;
+  int dev = 0;
+  if ((st = current_device(&dev))) return st;
+  return launched(nf4k::launch_embed_rows(E->codes, E->scales, E->M, E->K, ids, n, out, ot == NF4_BF16, codebook(),
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                  what);
 }
 
 

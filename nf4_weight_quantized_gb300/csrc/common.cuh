@@ -86,6 +86,7 @@ constexpr uint32_t kWaitPolls = 1u << 22;
 // registers the unit's reader with the library (nf4_check_device_errors).
 static __device__ unsigned int g_nf4_device_error;
 constexpr unsigned int kErrWaitTimeout = 1u;
+constexpr unsigned int kErrBadIndex = 2u;  // a token id outside its table (nf4_dequant_rows)
 
 using DeviceErrorReader = unsigned int (*)();
 void register_device_error_reader(DeviceErrorReader f);  // abi.cu
@@ -401,6 +402,8 @@ cudaError_t launch_quantize(const float* W, int64_t M, int64_t K, uint8_t* codes
                             const Codebook& cb, cudaStream_t s, int device);
 
 // Prefill chunk (chunk.cu).
+cudaError_t launch_embed_rows(const uint8_t* codes, const float* scales, int64_t V, int64_t K, const int64_t* ids,
+                              int64_t n, void* out, bool out_bf16, const Codebook& cb, cudaStream_t s);
 cudaError_t launch_chunk(const uint8_t* codes, const float* scales, int M, int K, const uint16_t* X, int N,
                          float* Y, void* workspace, const Codebook& cb, cudaStream_t s, int device);
 size_t chunk_workspace_bytes(int64_t M, int64_t K, int N);

@@ -25,7 +25,7 @@ MAX_K = 65536
 MAX_CHUNK_N = 32
 
 _STATUS = {0: "NF4_OK", -1: "NF4_EINVAL", -2: "NF4_EALIGN", -3: "NF4_ENULL", -4: "NF4_ECUDA", -5: "NF4_EARCH",
-           -6: "NF4_ETIMEOUT"}
+           -6: "NF4_ETIMEOUT", -7: "NF4_ERANGE"}
 
 
 class NF4Error(RuntimeError):
@@ -53,6 +53,7 @@ def _load():
         "nf4_gemv_residual": [W, P, I, P, P, P],
         "nf4_gemv_swiglu": [W, W, P, I, P, P],
         "nf4_gemv_qkv": [W, W, W, P, P, P, P, I, P, P, P, P],
+        "nf4_dequant_rows": [W, P, ctypes.c_int64, P, I, P],
         "nf4_gemv_argmax": [W, P, I, P, P, P, P],
         "nf4_gemm_chunk": [W, P, I, P, P, P],
         "nf4_gemm_chunk_noalloc": [W, P, I, P, P],
@@ -79,7 +80,8 @@ lib = _load()
 
 EXPORTS = ("nf4_gemv", "nf4_gemv_residual", "nf4_gemv_swiglu", "nf4_gemv_argmax", "nf4_gemm_chunk",
            "nf4_workspace_bytes", "nf4_quantize", "nf4_codebook", "nf4_last_error", "nf4_describe_config",
-           "nf4_check_device_errors", "nf4_gemm_chunk_noalloc", "nf4_gemv_qkv")
+           "nf4_check_device_errors", "nf4_gemm_chunk_noalloc", "nf4_gemv_qkv",
+           "nf4_dequant_rows")
 
 
 def _check(status: int):
@@ -194,6 +196,19 @@ def nf4_gemv_qkv(Wq: NF4Weight, Wk: NF4Weight, Wv: NF4Weight, x: torch.Tensor, b
     return tuple(outs)
 
 
+def nf4_dequant_rows(E: NF4Weight, ids: torch.Tensor, out: torch.Tensor | None = None,
+                     dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """Rows E_hat[ids] of an NF4 table, [len(ids), K], fp32 (exact) or bf16."""
+    n = ids.numel()
+    if out is None:
+        out = torch.empty((n, E.K), dtype=dtype, device=ids.device)
+    ot = _xtype(out)
+    e = E.struct()
+    _check(lib.nf4_dequant_rows(ctypes.byref(e), _dev(ids, "ids", torch.int64, n) if n else None, n,
+                                _dev(out, "out", out.dtype, n * E.K) if n else None, ot, _stream(stream)))
+    return out
+
+
 def nf4_workspace_bytes(M: int, K: int, N: int = 1) -> int:
     return int(lib.nf4_workspace_bytes(M, K, N))
 
@@ -261,7 +276,8 @@ def nf4_describe_config(M: int, K: int, N: int = 1) -> str:
 
 
 def nf4_check_device_errors() -> None:
-    """Synchronize and raise NF4Error(NF4_ETIMEOUT) if a kernel's bounded wait ran out."""
+    """Synchronize; raise NF4Error(NF4_ETIMEOUT) if a kernel's bounded wait ran out, or
+    NF4Error(NF4_ERANGE) if nf4_dequant_rows met an id outside its table."""
     _check(lib.nf4_check_device_errors())
 
 

@@ -83,7 +83,7 @@ def silu_product_bf16(seed: int, tid_a: int, tid_b: int, n: int) -> np.ndarray:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "gemv", "residual", "swiglu", "argmax", "chunk", "qkv"
+    kind: str  # "gemv", "residual", "swiglu", "argmax", "chunk", "qkv", "embed"
     M: int
     K: int
     N: int
@@ -109,6 +109,8 @@ WORKLOADS = {
     "qkv3b": Workload("qkv3b", "qkv", 2048, 2048, 1, 5, "bf16",
                       "3B q/k/v 2048x2048 + 2x 256x2048 in one launch, x bf16 N(0,1), fp32 biases N(0,1)",
                       M_kv=256),
+    "embed_prefill": Workload("embed_prefill", "embed", 151936, 2048, 4096, 6, "bf16",
+                              "3B embedding table 151936x2048 kept as NF4, 4096 token ids uniform, bf16 rows out"),
 }
 
 
@@ -122,7 +124,10 @@ def workload_inputs(w: Workload, M: int | None = None) -> dict:
     K = w.K
     s = w.seed
     d = {}
-    if w.kind == "qkv":
+    if w.kind == "embed":
+        d["W"] = weights(s, 0, M, K)
+        d["ids"] = token_ids(s, 1, w.N, M)
+    elif w.kind == "qkv":
         d["W"] = weights(s, 0, M, K)
         d["Wk"] = weights(s, 1, w.M_kv, K)
         d["Wv"] = weights(s, 2, w.M_kv, K)
