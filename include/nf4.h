@@ -31,6 +31,12 @@
  *   - Inputs are never written, except that nf4_gemv_residual's `y` may alias
  *     `residual`.  Any other overlap between an output and an input is
  *     undefined behaviour.
+ *   - N=1 kernels use programmatic dependent launch: they may start, and read
+ *     (or prefetch) the weights, before the previous kernel on the stream has
+ *     finished when that kernel allows it; activations and outputs are touched
+ *     only after it finishes.  So weights must not be written by the kernel
+ *     launched just before on the same stream if that kernel triggers its
+ *     dependents early (no kernel of this library that writes weights does).
  *   - Arguments are validated on the host before any launch; a failed call
  *     launches nothing and returns a negative nf4_status.  nf4_last_error()
  *     gives a message for the calling thread's last failure.  Kernels do not

@@ -206,6 +206,16 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
     }
     a.M = (int)end;
   }
+  if (!use_register_kernel()) {
+    const nf4k::ClusterConfig cc = nf4k::choose_cluster_config(epi, a.M, W->K, dev);
+    if (cc.ok) {
+      const cudaError_t e = nf4k::launch_gemv_cluster(epi, xt == NF4_BF16, a, cc, reinterpret_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess)
+        return fail(NF4_ECUDA, "%s: launch failed (cluster kernel, %d clusters of %d blocks x %d threads): %s%s", what,
+                    cc.clusters, cc.CL, cc.threads, cudaGetErrorString(e), nf4k::take_launch_note().c_str());
+      return NF4_OK;
+    }
+  }
   const bool scales16 = aligned(W->scales, 16) && (!W2 || aligned(W2->scales, 16)) && scales16_extra;
   if (scales16 && !use_register_kernel()) {
     const nf4k::TmaConfig tc = nf4k::choose_tma_config(epi, xt == NF4_BF16, a.M, W->K, dev);
@@ -449,7 +459,15 @@ const char* nf4_describe_config(int64_t M, int64_t K, int N) {
     return g_describe.c_str();
   }
   char buf[512];
-  if (N == 1) {
+  const nf4k::ClusterConfig cc =
+      (N == 1 && !use_register_kernel()) ? nf4k::choose_cluster_config(nf4k::EPI_PLAIN, M, K, dev) : nf4k::ClusterConfig{};
+  if (cc.ok) {
+    std::snprintf(buf, sizeof buf,
+                  "gemv M=%lld K=%lld: cluster split-K kernel, %d clusters of %d blocks (K split %d ways, %d rows per "
+                  "cluster), %d threads per block, partial sums added through distributed shared memory, %s",
+                  (long long)M, (long long)K, cc.clusters, cc.CL, cc.CL, cc.RPC, cc.threads,
+                  nf4k::pdl_enabled() ? "programmatic dependent launch" : "plain launch");
+  } else if (N == 1) {
     const nf4k::TmaConfig t = use_register_kernel() ? nf4k::TmaConfig{} : nf4k::choose_tma_config(nf4k::EPI_PLAIN, true, M, K, dev);
     if (t.ok) {
       std::snprintf(buf, sizeof buf,

@@ -393,6 +393,16 @@ struct TmaConfig {
   int subr, nb;  // rows per full barrier in the stage, full barriers per stage
 };
 TmaConfig choose_tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int device);
+
+// Cluster split-K kernel for few rows (gemv_cluster.cu).
+struct ClusterConfig {
+  bool ok;       // the epilogue and shape qualify
+  int CL;        // blocks per cluster (K split)
+  int RPC;       // rows per cluster
+  int clusters, threads, smem;
+};
+ClusterConfig choose_cluster_config(int epi, int64_t M, int64_t K, int device);
+cudaError_t launch_gemv_cluster(int epi, bool x_bf16, const GemvArgs& a, const ClusterConfig& c, cudaStream_t s);
 cudaError_t launch_gemv_tma(int epi, bool x_bf16, const GemvArgs& a, const TmaConfig& c, cudaStream_t s);
 
 // Host launchers (gemv.cu / quantize.cu).

@@ -401,3 +401,34 @@ def test_qkv_errors(nf4):
     x = H.x_tensor(H.make_x(740, 512, "bf16"))
     with pytest.raises(nf4.NF4Error, match="share K"):
         nf4.nf4_gemv_qkv(W, W2, W, x)
+
+
+# ------------------------------------------------- cluster split-K, few rows
+
+
+@pytest.mark.parametrize("M,K", [(256, 2048), (2048, 2048), (1, 64), (77, 5120), (3000, 2048), (5, 8192)])
+def test_cluster_kernel_and_bulk_copy_agree_with_oracle(nf4, M, K, monkeypatch):
+    # few rows, opt-in (NF4_CLUSTER=1): K split across a thread-block cluster,
+    # partials added through distributed shared memory; by default the same
+    # call takes the bulk-copy kernel.  Both are checked against the oracle.
+    monkeypatch.setenv("NF4_CLUSTER", "1")
+    seed = 750 + M
+    codes, scales = H.quantized(seed, 0, M, K)
+    x = H.make_x(seed, K, "bf16")
+    r = synth.normal_f32(seed, 3, M)
+    y_ref, S = oracle.gemv(codes, scales, x)
+    yr64, _ = oracle.gemv_residual(codes, scales, x, r)
+    W = H.weight_tensors(codes, scales)
+    assert "cluster" in nf4.nf4_describe_config(M, K, 1)
+    y1 = nf4.nf4_gemv(W, H.x_tensor(x)).cpu().numpy()
+    H.assert_within(y1, y_ref, S, what=f"cluster {M}x{K}")
+    yr = nf4.nf4_gemv_residual(W, H.x_tensor(x), torch.from_numpy(r).cuda()).cpu().numpy()
+    H.assert_within(yr, yr64, S, extra=H.ulp_f32(yr64), what=f"cluster residual {M}x{K}")
+    xf = H.make_x(seed, K, "f32")
+    yf_ref, Sf = oracle.gemv(codes, scales, xf)
+    H.assert_within(nf4.nf4_gemv(W, H.x_tensor(xf)).cpu().numpy(), yf_ref, Sf, what=f"cluster f32 {M}x{K}")
+    monkeypatch.setenv("NF4_CLUSTER", "0")
+    assert "cluster" not in nf4.nf4_describe_config(M, K, 1)
+    y2 = nf4.nf4_gemv(W, H.x_tensor(x)).cpu().numpy()
+    H.assert_within(y2, y_ref, S, what=f"bulk-copy {M}x{K}")
+    nf4.nf4_check_device_errors()
