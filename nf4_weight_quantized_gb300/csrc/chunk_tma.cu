@@ -18,7 +18,7 @@
 //  * sixteen dequantizing warps turn each 64-column k-tile of codes into the bf16
 //    A operand (fp32 level x fp32 scale from the lane-replicated pair table,
 //    rounded once) and store it straight into tensor memory (tcgen05.st; row m
-//    in TMEM lane m), a ring of three stages of two k-tiles: the A operand never passes
+//    in TMEM lane m), a ring of three stages of four k-tiles: the A operand never passes
 //    through shared memory, which the pair-table reads alone keep busy;
 //  * one thread issues tcgen05.mma (M = 128, N = 32, K = 16, A from TMEM, X from
 //    shared memory) into one of two 32-column TMEM accumulators, so four
@@ -66,7 +66,10 @@ constexpr int SA = NF4_CHUNK_SA;  // A stages in tensor memory, KS k-tiles each
 // Measured alone, a wait + fence costs about 190 cycles and a commit 44
 // against 45 per M=128 N=32 K=16 MMA, so one handshake per k-tile would cost
 // more than the k-tile's tensor-core work.
-constexpr int KS = 2;
+#ifndef NF4_CHUNK_KS
+#define NF4_CHUNK_KS 4
+#endif
+constexpr int KS = NF4_CHUNK_KS;
 static_assert(KQ % KS == 0, "A stages tile a unit");
 constexpr int CODES_BYTES = TM * KQ * KT / 2;    // 16 KB
 constexpr int XT_BYTES = TN * KT * 2;            // 4 KB per k-tile
@@ -78,7 +81,7 @@ static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory per block");
 // columns (64 bf16 of each row per k-tile, two per 32-bit column)
 constexpr int A_COLS = KS * KT / 2;
 constexpr int A_COL0 = 2 * TN;
-constexpr int TMEM_COLS = 256;
+constexpr int TMEM_COLS = (A_COL0 + SA * A_COLS) <= 256 ? 256 : 512;  // a power of two; one block per SM
 static_assert(A_COL0 + SA * A_COLS <= TMEM_COLS, "tensor memory per block");
 constexpr int PLAN_SMS = 152;  // blocks planned for a 152-SM GB300 (the workspace depends on the shape only)
 
@@ -361,10 +364,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int h = 0; h < KQ / KS; ++h, ++j) {
         const int as = j % SA;
-        uint32_t p[KS][8];
+        // the tensor core has finished with this A stage's previous contents
+        if (j >= SA) mbar_wait_warp(a_empty(as), (uint32_t)(((j / SA) - 1) & 1), abort, lane, NF4_DQ_SLEEP);
+        tc_fence_after_sync();
 #pragma unroll
         for (int i2 = 0; i2 < KS; ++i2) {
           const int i = h * KS + i2;
+          uint32_t p[8];
           const uint2 cw = lds64(raw + r * 128 + (((2 * i + (cg >> 1)) ^ (r & 7)) << 4) + (cg & 1) * 8);
           const uint32_t w2[2] = {cw.x, cw.y};
 #pragma unroll
@@ -375,15 +381,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               const float2 v = *reinterpret_cast<const float2*>(smem + off);
               float w0, w1;
               mul2_f32(w0, w1, v.x, v.y, scl[i]);  // two IEEE products, as v.x * s and v.y * s
-              p[i2][4 * e + jj] = pack_bf16x2(w0, w1);
+              p[4 * e + jj] = pack_bf16x2(w0, w1);
             }
+          tmem_st_32x32b_x8(tmem + lane_base + (uint32_t)(A_COL0 + as * A_COLS + i2 * (KT / 2) + cg * 8), p);
         }
-        // the tensor core has finished with this A stage's previous contents
-        if (j >= SA) mbar_wait_warp(a_empty(as), (uint32_t)(((j / SA) - 1) & 1), abort, lane, NF4_DQ_SLEEP);
-        tc_fence_after_sync();
-#pragma unroll
-        for (int i2 = 0; i2 < KS; ++i2)
-          tmem_st_32x32b_x8(tmem + lane_base + (uint32_t)(A_COL0 + as * A_COLS + i2 * (KT / 2) + cg * 8), p[i2]);
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
