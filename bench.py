@@ -354,6 +354,25 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------- GPU arm
 
+def reduce_max(dist, v: float, device=None) -> float:
+    """Max over ranks of a per-rank value (the slowest replica's time); the
+    value itself without a process group.  NCCL needs a device tensor, gloo a
+    CPU one."""
+    if dist is None:
+        return v
+    import torch
+
+    t = torch.tensor([v], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(world: int, bytes_per_call: int, calls: int, max_secs: float) -> float:
+    """Whole-job throughput in GB/s: every replica moved `bytes_per_call` per
+    call, timed by the slowest replica."""
+    return world * bytes_per_call * calls / max_secs / 1e9
+
+
 def run_gpu(args, rank, world, dist):
     import torch
 
@@ -369,12 +388,9 @@ def run_gpu(args, rank, world, dist):
     sampler = ClockSampler(local)
     secs, clocks = time_calls(torch, call, copies, args.steps, args.warmup, stream, dist,
                               clock_window_s=args.clock_window, sampler=sampler)
-    if dist is not None:
-        t = torch.tensor([secs], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
+    secs = reduce_max(dist, secs, device)
     per_call = secs / args.steps
-    value = world * b["weight"] * args.steps / secs / 1e9
+    value = replica_value(world, b["weight"], args.steps, secs)
     achieved = b["total"] / per_call / 1e9
 
     # e2e through the public API with host buffers
@@ -405,11 +421,8 @@ def run_gpu(args, rank, world, dist):
         e1.record(stream)
     stream.synchronize()
     e2e_secs = e0.elapsed_time(e1) / 1e3
-    if dist is not None:
-        t = torch.tensor([e2e_secs], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_secs = float(t.item())
-    e2e = {"value": world * b["weight"] * n_e2e / e2e_secs / 1e9, "unit": UNIT,
+    e2e_secs = reduce_max(dist, e2e_secs, device)
+    e2e = {"value": replica_value(world, b["weight"], n_e2e, e2e_secs), "unit": UNIT,
            "h2d_bytes_per_step": x_host.numel() * 2 + r_host.numel() * 4,
            "d2h_bytes_per_step": y_host.numel() * 4, "steps": n_e2e,
            "us_per_step": e2e_secs / n_e2e * 1e6}

@@ -1,0 +1,100 @@
+"""Host logic of the benchmark and the library, no GPU: the replica
+aggregation bench.py uses for N > 1 (world-size-2 gloo process group on the
+CPU), algorithmic byte counts, workspace sizes, and the input generators."""
+from __future__ import annotations
+
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from nf4_weight_quantized_gb300 import synth
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _replica(rank: int, world: int, port: int, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        secs = 1.0 + 0.5 * rank  # rank 1 is the slow replica
+        m = bench.reduce_max(dist, secs)
+        q.put((rank, m, bench.replica_value(world, 12_719_616, 100, m)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replicas_take_the_slowest_rank_gloo():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_replica, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(world))
+    for rank, m, value in got:
+        assert m == 1.5  # both ranks see the max
+        assert value == pytest.approx(2 * 12_719_616 * 100 / 1.5 / 1e9)
+
+
+def test_reduce_max_without_a_process_group():
+    assert bench.reduce_max(None, 3.25) == 3.25
+    assert bench.replica_value(1, 10**9, 2, 2.0) == 1.0
+
+
+def test_algorithmic_bytes():
+    # codes K/2 + scales K/16 per row
+    assert bench.bytes_of("residual", 2048, 11008)["total"] == 2048 * 11008 * 9 // 16 + 11008 * 2 + 2048 * 8
+    assert bench.bytes_of("swiglu", 11008, 2048)["weight"] == 2 * 11008 * 2048 * 9 // 16
+    assert bench.bytes_of("argmax", 151936, 2048)["total"] == 151936 * 2048 * 9 // 16 + 4096 + 151936 * 4 + 8
+    assert bench.bytes_of("chunk", 13824, 5120, 32)["total"] == 13824 * 5120 * 9 // 16 + 32 * 5120 * 2 + 32 * 13824 * 4
+    qkv = bench.bytes_of("qkv", 2048, 2048, 1, 256)
+    assert qkv["weight"] == 2560 * 2048 * 9 // 16 and qkv["total"] == qkv["weight"] + 4096 + 2560 * 8
+    e = bench.bytes_of("embed", 151936, 2048, 4096)
+    assert e["weight"] == 4096 * 1152 and e["total"] == 4096 * 1152 + 4096 * 8 + 4096 * 2048 * 2
+
+
+def test_workload_inputs_are_seeded():
+    w = synth.WORKLOADS["qkv3b"]
+    a, b = synth.workload_inputs(w), synth.workload_inputs(w)
+    assert set(a) == {"W", "Wk", "Wv", "x", "bq", "bk", "bv"}
+    assert all(np.array_equal(a[k], b[k]) for k in a)
+    ids = synth.token_ids(6, 1, 4096, 151936)
+    assert ids.dtype == np.int64 and ids.min() >= 0 and ids.max() < 151936
+    assert np.array_equal(ids, synth.token_ids(6, 1, 4096, 151936))
+
+
+def test_chunk_workspace_sizes(nf4_lib):
+    nf4 = nf4_lib
+    # 14B-shaped chunk: partials + one ticket per 128-row tile, within the no-alloc scratch
+    n = nf4.nf4_workspace_bytes(13824, 5120, 32)
+    assert 16 < n <= 8 << 20
+    # many tiles per block: whole tiles, no partials (argmax-sized workspace)
+    assert nf4.nf4_workspace_bytes(151936, 2048, 1) == 16
+    # K % 256 != 0 (fallback kernel only) still has its split-K partials
+    assert nf4.nf4_workspace_bytes(13824, 5056, 32) > 16
+
+
+@pytest.fixture(scope="module")
+def nf4_lib():
+    from nf4_weight_quantized_gb300 import build
+
+    if not os.path.exists(build.library_path()):
+        build.build()
+    from nf4_weight_quantized_gb300 import nf4 as mod
+
+    return mod
