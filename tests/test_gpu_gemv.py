@@ -432,3 +432,13 @@ def test_cluster_kernel_and_bulk_copy_agree_with_oracle(nf4, M, K, monkeypatch):
     y2 = nf4.nf4_gemv(W, H.x_tensor(x)).cpu().numpy()
     H.assert_within(y2, y_ref, S, what=f"bulk-copy {M}x{K}")
     nf4.nf4_check_device_errors()
+
+
+@pytest.mark.parametrize("Ms,K", [((300, 70, 130), 512), ((2048, 256, 256), 2048)])
+def test_qkv_cluster_kernel(nf4, Ms, K, monkeypatch):
+    # the opt-in cluster split-K kernel with the fused q/k/v epilogue
+    monkeypatch.setenv("NF4_CLUSTER", "1")
+    assert "cluster" in nf4.nf4_describe_config(sum(Ms), K, 1)
+    _qkv_case(nf4, Ms, K, "bf16", (True, False, True), 760 + K)
+    _qkv_case(nf4, Ms, K, "f32", (True, True, True), 761 + K)
+    nf4.nf4_check_device_errors()
