@@ -47,6 +47,7 @@ def load():
     lib.nf4o_gemm_chunk.argtypes = [P, P, I64, I64, P, I64, P, I64, P, P]
     lib.nf4o_gemv_qkv.argtypes = [P, P, P, P, I64, P, I, P, I64, P, P]
     lib.nf4o_dequant_rows.argtypes = [P, P, I64, I64, P, I64, P, P, P]
+    lib.nf4o_gemv_glu_interleaved.argtypes = [P, P, I64, I64, P, I, P, I64, P, P, P, P]
     lib.nf4o_round_bf16.argtypes = [ctypes.c_double]
     lib.nf4o_round_bf16.restype = ctypes.c_uint16
     for name in ("nf4o_codebook", "nf4o_quantize", "nf4o_dequant", "nf4o_gemv", "nf4o_gemv_residual",
@@ -183,6 +184,26 @@ def gemv_swiglu(g_codes, g_scales, u_codes, u_scales, x, rows=None):
     u = np.zeros(n, np.float64)
     _check(load().nf4o_gemv_swiglu(*[_ptr(a) for a in args], M, K, _ptr(x), _xtype(x), _ptr(r), n,
                                    _ptr(o64), _ptr(obf), _ptr(g), _ptr(u)), "gemv_swiglu")
+    return o64, obf, g, u
+
+
+def gemv_glu_interleaved(codes, scales, x, cols=None):
+    """SwiGLU over one matrix whose rows alternate gate (even) and up (odd).
+
+    Returns (float64 silu(g)*u, bf16 bits of it, float64 g, float64 u) for the
+    outputs ``cols`` (all ``M2 / 2`` if None).
+    """
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    x = np.ascontiguousarray(x)
+    M2, K = codes.shape[0], codes.shape[1] * 2
+    c, n = _rows(cols, M2 // 2)
+    o64 = np.zeros(n, np.float64)
+    obf = np.zeros(n, np.uint16)
+    g = np.zeros(n, np.float64)
+    u = np.zeros(n, np.float64)
+    _check(load().nf4o_gemv_glu_interleaved(_ptr(codes), _ptr(scales), M2, K, _ptr(x), _xtype(x), _ptr(c), n,
+                                            _ptr(o64), _ptr(obf), _ptr(g), _ptr(u)), "gemv_glu_interleaved")
     return o64, obf, g, u
 
 

@@ -12,6 +12,8 @@
  *   SwiGLU = silu(gate) * up with SiLU applied to the full gate sum; greedy id =
  *   argmax of the logits), section 6 "Linear primitive" (FP32 LUT x scale x x;
  *   N=1 takes a [K] view; o/down add a residual into y; prefill chunks of 32).
+ * Gate/up rows interleaved in one matrix: "gizai:tensor/lazy", method
+ *   Lazy.gluIn (output column c = silu of row 2c times row 2c + 1).
  * Argmax tie rule: golang.design/x/accel/tensor, "func Argmax", paragraph
  *   "Ties go to the lowest index".
  * bf16 -> f32 widening is exact: same page, "func Cast", "bf16 widens and does
@@ -335,6 +337,38 @@ int nf4o_gemv_swiglu(const uint8_t* g_codes, const float* g_scales, const uint8_
     st = nf4o_gemv(u_codes, u_scales, M, K, x, xt, &m, 1, &us, NULL);
     if (st) return st;
     double v = silu(gs) * us;
+    if (out_f64) out_f64[i] = v;
+    if (out_bf16) out_bf16[i] = f64_to_bf16_bits(v);
+    if (g) g[i] = gs;
+    if (u) u[i] = us;
+  }
+  return NF4O_OK;
+}
+
+/*
+ * SwiGLU over one matrix whose rows alternate gate and up ("gizai:tensor/lazy",
+ * method Lazy.gluIn: output column c is silu of product row 2c times product
+ * row 2c + 1).  The matrix has M2 = 2 x outputs rows; v = W x in float64 as
+ * nf4o_gemv; out[c] = silu(v[2c]) * v[2c + 1], rounded once to bf16 as
+ * nf4o_gemv_swiglu.  `cols` (or all M2 / 2 outputs when NULL) selects outputs;
+ * any output array may be NULL.  An odd M2 is rejected.
+ */
+int nf4o_gemv_glu_interleaved(const uint8_t* codes, const float* scales, int64_t M2, int64_t K, const void* x,
+                              int xt, const int64_t* cols, int64_t ncols, double* out_f64, uint16_t* out_bf16,
+                              double* g, double* u) {
+  if (M2 < 2 || (M2 & 1)) return NF4O_EINVAL;
+  const int64_t n_out = M2 / 2;
+  if (!cols) ncols = n_out;
+  for (int64_t i = 0; i < ncols; ++i) {
+    const int64_t c = cols ? cols[i] : i;
+    if (c < 0 || c >= n_out) return NF4O_EINVAL;
+    int64_t rg = 2 * c, ru = 2 * c + 1;
+    double gs, us;
+    int st = nf4o_gemv(codes, scales, M2, K, x, xt, &rg, 1, &gs, NULL);
+    if (st) return st;
+    st = nf4o_gemv(codes, scales, M2, K, x, xt, &ru, 1, &us, NULL);
+    if (st) return st;
+    const double v = silu(gs) * us;
     if (out_f64) out_f64[i] = v;
     if (out_bf16) out_bf16[i] = f64_to_bf16_bits(v);
     if (g) g[i] = gs;

@@ -10,7 +10,9 @@ fused q/k/v: a worked example with distinct closed-form values per segment, zero
 scales giving exactly the bias, row sampling across the segment boundaries;
 embedding rows: a worked example with exact values and bf16 bits, out-of-range
 ids giving zero rows, bf16 equal to round-to-nearest-even on the bit pattern;
-argmax ties go to the lowest index ("golang.design/x/accel/tensor", func Argmax).
+argmax ties go to the lowest index ("golang.design/x/accel/tensor", func Argmax);
+SwiGLU with gate/up rows interleaved: a worked example using silu(0) = 0 and
+silu(z) - silu(-z) = z, and equality with the two-matrix SwiGLU.
 Chunk: equals the GEMV exactly when every W_hat is representable in bf16, and
 otherwise stays within the bf16 rounding bound of the weights.
 """
@@ -560,3 +562,61 @@ def test_dequant_rows_bf16_is_round_to_nearest_even(oracle_mod):
     u = f32.view(np.uint32).astype(np.uint64)
     rne = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
     assert np.array_equal(b16, rne)
+
+
+# ------------------------------------------- SwiGLU, gate/up rows interleaved
+# "gizai:tensor/lazy", method Lazy.gluIn: output column c is silu(v[2c]) times
+# v[2c + 1], v the product of one matrix whose rows alternate gate and up.
+
+
+def test_glu_interleaved_worked_example(oracle_mod, cb):
+    # K = 64, x = 1.  Rows (level, scale): 0: (+1, 0.5) -> g0 = 32;
+    # 1: (-1, 0.25) -> u0 = -16; 2: (0, 9) -> g1 = 0; 3: (+1, 2) -> u1 = 128;
+    # 4: (-1, 0.5) -> g2 = -32; 5: (-1, 0.25) -> u2 = -16.
+    # silu(0) = 0, so out1 = 0 exactly.  silu(z) - silu(-z) = z for every z
+    # (z s(z) + z s(-z) = z, s the logistic function), so out0 - out2 = 32 u0
+    # = -512 up to float64 rounding of the two products.  Applying silu to the
+    # up rows instead, or pairing rows (2c+1, 2c+2), breaks both.
+    assert cb[15] == 1.0 and cb[0] == -1.0 and cb[7] == 0.0
+    K = 64
+    byte = {1: 0xFF, -1: 0x00, 0: 0x77}
+    spec = [(1, 0.5), (-1, 0.25), (0, 9.0), (1, 2.0), (-1, 0.5), (-1, 0.25)]
+    codes = np.stack([np.full(K // 2, byte[lv], np.uint8) for lv, _ in spec])
+    scales = np.array([[s] for _, s in spec], np.float32)
+    out, obf, g, u = oracle_mod.gemv_glu_interleaved(codes, scales, np.ones(K, np.float32))
+    assert list(g) == [32.0, 0.0, -32.0] and list(u) == [-16.0, 128.0, -16.0]
+    assert out[1] == 0.0 and obf[1] in (0, 0x8000)
+    assert abs((out[0] - out[2]) - (-512.0)) <= 1e-12
+    # out0 = -16 * 32 / (1 + e^-32): within 1e-13 of -512; bf16 of it is -512
+    assert abs(out[0] + 512.0) < 1e-10 and obf[0] == 0xC400
+    assert 0.0 < out[2] < 1e-10  # -16 * silu(-32), silu(-32) ~ -4e-13
+
+
+def test_glu_interleaved_equals_two_matrices(oracle_mod):
+    # the interleaved layout is the two-matrix SwiGLU with gate = even rows and
+    # up = odd rows, value for value
+    M, K = 40, 320
+    Wg = synth.weights(95, 0, M, K)
+    Wu = synth.weights(95, 1, M, K)
+    W = np.empty((2 * M, K), np.float32)
+    W[0::2], W[1::2] = Wg, Wu
+    codes, scales = oracle_mod.quantize(W)
+    x = synth.normal_bf16(95, 2, K)
+    out, obf, g, u = oracle_mod.gemv_glu_interleaved(codes, scales, x)
+    ref = oracle_mod.gemv_swiglu(codes[0::2], scales[0::2], codes[1::2], scales[1::2], x)
+    for a, b in zip((out, obf, g, u), ref):
+        assert np.array_equal(a, b)
+    cols = [M - 1, 0, 17, 17]
+    sub = oracle_mod.gemv_glu_interleaved(codes, scales, x, cols=cols)
+    for a, b in zip(sub, (out, obf, g, u)):
+        assert np.array_equal(a, b[cols])
+
+
+def test_glu_interleaved_rejects_bad_shapes(oracle_mod):
+    K = 64
+    codes = np.full((3, K // 2), 0x77, np.uint8)
+    scales = np.ones((3, 1), np.float32)
+    with pytest.raises(ValueError):
+        oracle_mod.gemv_glu_interleaved(codes, scales, np.ones(K, np.float32))  # odd row count
+    with pytest.raises(ValueError):
+        oracle_mod.gemv_glu_interleaved(codes[:2], scales[:2], np.ones(K, np.float32), cols=[1])
