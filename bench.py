@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "NF4 GEMV effective weight GB/s (N=1, 3B down_proj 2048x11008 + residual)"
 UNIT = "GB/s"
 MAIN = "down_residual"
+WORKLOAD_NAME = "3B down_proj 2048x11008 NF4 (block 64, fp32 scales) + fp32 residual, x bf16, N=1"
 
 
 # ------------------------------------------------------------------ helpers
@@ -343,7 +344,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": "3B down_proj 2048x11008 + residual (bounded sample)",
+        "data": "synthetic", "config": {"workload": WORKLOAD_NAME, "parallelism": "single",
+                                        "sample": f"{rows_per_step} rows per step (rotating), full K",
                                         "rows_per_step": rows_per_step, "l2": "host"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{rows_per_step} rows x K=11008 per step, {args.steps} steps"},
@@ -456,8 +458,7 @@ def run_gpu(args, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": per_call * 1e3, "us_per_call": per_call * 1e6,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": "3B down_proj 2048x11008 NF4 (block 64, fp32 scales) + fp32 residual, "
-                               "x bf16, N=1",
+        "config": {"workload": WORKLOAD_NAME,
                    "l2": f"rotating {copies} weight copies ({copies * b['weight'] / 1e6:.0f} MB, >3x L2)",
                    "parallelism": "replicas" if world > 1 else "single",
                    "kernel": nf4.nf4_describe_config(2048, 11008, 1)},

@@ -1,6 +1,7 @@
 """Host logic of the benchmark and the library, no GPU: the replica
 aggregation bench.py uses for N > 1 (world-size-2 gloo process group on the
-CPU), algorithmic byte counts, workspace sizes, and the input generators."""
+CPU), algorithmic byte counts, workspace sizes, the input generators, and the
+reference arm's JSON line (the oracle timed on the host)."""
 from __future__ import annotations
 
 import os
@@ -98,3 +99,34 @@ def nf4_lib():
     from nf4_weight_quantized_gb300 import nf4 as mod
 
     return mod
+
+
+def _bench_lines(*args, env=None):
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], capture_output=True, text=True,
+                       cwd=root, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_reference_arm_line():
+    # the reference arm (the oracle on the host) prints one JSON line on the
+    # same metric, unit and workload as the GPU arm
+    lines = _bench_lines("--impl", "reference", "--steps", "2", "--warmup", "3")
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["config"]["workload"] == bench.WORKLOAD_NAME and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 2 and d["warmup"] >= 3 and d["n_gpus"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    assert _bench_lines("--impl", "reference", "--steps", "2", "--warmup", "3", env=env) == []
