@@ -3,7 +3,8 @@
 Codebook: the closed form of the QLoRA NormalFloat construction evaluated with
 scipy's inverse normal CDF (a library routine) and the table's invariants.
 Encoder: exact rational brute force, round trip, error bound, zero block.
-GEMV: hand-computed worked examples (tests/golden/worked_examples.txt), exact
+GEMV: hand-computed worked examples (tests/golden/worked_examples.txt), each
+code reading its own level (one-hot x against scipy's closed form), exact
 sums via math.fsum, numpy float64 matmul, power-of-two linearity, the zero level.
 Epilogues: residual / SwiGLU / argmax reduce to the GEMV plus their definitions;
 fused q/k/v: a worked example with distinct closed-form values per segment, zero
@@ -252,6 +253,29 @@ def test_sum_of_levels(oracle_mod, cb):
     y, S = oracle_mod.gemv(_pack(c), np.ones((1, 1), np.float32), np.ones(64, np.float32))
     assert y[0] == math.fsum(4 * [float(v) for v in cb])
     assert S[0] == math.fsum(4 * [abs(float(v)) for v in cb])
+
+
+def test_each_code_reads_its_own_level(oracle_mod):
+    # A permuted table would keep the sum of levels; this pins code -> level.
+    # Row c holds code c everywhere (both nibbles), scale 2^-3 in block 0 and
+    # 3 in block 1.  x = e_j picks one weight: y_c = level_c * scale, with the
+    # levels from the closed form of the construction (scipy's inverse normal
+    # CDF, independent of the oracle's bisection), rounded to fp32, times a
+    # scale; the fp32 product is exact for 2^-3 and rounded once for 3.
+    ndtri = pytest.importorskip("scipy.special").ndtri
+    d = 0.5 * (1 / 32 + 1 / 30)
+    lv = np.sort(np.concatenate([ndtri(1 - d - np.arange(8) * (0.5 - d) / 8),
+                                 ndtri(d + np.arange(7) * (0.5 - d) / 7), [0.0]])) / ndtri(1 - d)
+    lv = lv.astype(np.float32)
+    K = 128
+    codes = np.repeat((np.arange(16, dtype=np.uint8) * 0x11)[:, None], K // 2, axis=1)
+    scales = np.tile(np.array([[0.125, 3.0]], np.float32), (16, 1))
+    for j, s in ((0, 0.125), (1, 0.125), (63, 0.125), (64, 3.0), (127, 3.0)):
+        x = np.zeros(K, np.float32)
+        x[j] = 1.0
+        y, _ = oracle_mod.gemv(codes, scales, x)
+        want = (lv * np.float32(s)).astype(np.float64)  # one fp32 rounding of the product
+        assert np.array_equal(y, want), (j, y, want)
 
 
 def test_gemv_exact_sum(oracle_mod):
