@@ -118,3 +118,14 @@ def test_noalloc_rejects_oversize_before_any_device_work(nf4):
     st = nf4.lib.nf4_gemm_chunk_noalloc(ctypes.byref(nf4.nf4_weight(4096, 4096, 8, 100)), ctypes.c_void_p(4096), 4,
                                         ctypes.c_void_p(4096), None)
     assert st == -1 and "multiple of 64" in nf4.nf4_last_error()
+
+
+def test_c_program_uses_the_abi_without_python(tmp_path):
+    # a plain C caller: codebook, argument checks and workspace sizes through
+    # include/nf4.h and libnf4.so alone (no device needed)
+    from .c.build_c import build_abi_program
+
+    exe = build_abi_program(str(tmp_path))
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert "host checks ok" in r.stdout
