@@ -137,7 +137,7 @@ def bytes_of(kind: str, M: int, K: int, N: int = 1, M_kv: int = 0) -> dict:
         tot = w + K * 2 + M * 4 + M * 4  # + biases + outputs
     elif kind == "residual":
         tot = w + K * 2 + M * 4 + M * 4
-    elif kind == "swiglu":
+    elif kind in ("swiglu", "glu"):  # glu: M outputs of a 2 M-row matrix
         w *= 2
         tot = w + K * 2 + M * 2
     elif kind == "argmax":
@@ -154,7 +154,8 @@ def describe(nf4, w) -> str:
     if w.kind == "embed":
         return (f"nf4_dequant_rows: {w.N} rows of a {w.M}x{w.K} NF4 table, bf16 out, one thread per 32 weights, "
                 "256-thread blocks")
-    return nf4.nf4_describe_config(w.M + 2 * w.M_kv, w.K, w.N)
+    rows = 2 * w.M if w.kind == "glu" else w.M + 2 * w.M_kv
+    return nf4.nf4_describe_config(rows, w.K, w.N)
 
 
 def build_calls(name: str, torch, nf4, synth, device, copies=None):
@@ -200,6 +201,12 @@ def build_calls(name: str, torch, nf4, synth, device, copies=None):
         out = torch.empty(M, dtype=torch.bfloat16, device=device)
         call = lambda i, s: nf4.nf4_gemv_swiglu(Wg[i % copies], Wu[i % copies], x, out, stream=s)
         ctx = {"Wg": Wg, "Wu": Wu, "x": x, "out": out}
+    elif w.kind == "glu":
+        Ws = replicate(quant(d["W"]))
+        x = bf16(d["x"])
+        out = torch.empty(M, dtype=torch.bfloat16, device=device)
+        call = lambda i, s: nf4.nf4_gemv_glu_interleaved(Ws[i % copies], x, out, stream=s)
+        ctx = {"W": Ws, "x": x, "out": out}
     elif w.kind == "argmax":
         Ws = replicate(quant(d["W"]))
         x = bf16(d["x"])
@@ -433,7 +440,7 @@ def run_gpu(args, rank, world, dist):
 
     workloads = {}
     if args.all_workloads:
-        for name in ("swiglu", "lm_head_argmax", "gemv14b", "chunk14b", "qkv3b", "embed_prefill"):
+        for name in ("swiglu", "glu3b", "lm_head_argmax", "gemv14b", "chunk14b", "qkv3b", "embed_prefill"):
             try:
                 c2, cp2, b2, ctx2 = build_calls(name, torch, nf4, synth, device)
                 n2 = args.workload_steps

@@ -119,6 +119,19 @@ nf4_status nf4_gemv_swiglu(const nf4_weight* Wg, const nf4_weight* Wu, const voi
                            uint16_t* out, nf4_stream stream);
 
 /*
+ * SwiGLU over one matrix whose rows alternate gate and up:
+ *   out[c] = bf16( silu(v[2c]) * v[2c + 1] ),  v = W . x
+ * Source: "gizai:tensor/lazy", method Lazy.gluIn (a gate and an up projection
+ * with their rows interleaved; output column c is silu of row 2c times row
+ * 2c + 1, made as the product is stored, so v itself is never written).  The
+ * arithmetic is that of nf4_gemv_swiglu.
+ *   W       weight of 2 x outputs rows (W->M even, else NF4_EINVAL), M x K
+ *   out     [W->M / 2] bf16 bits, round to nearest even
+ */
+nf4_status nf4_gemv_glu_interleaved(const nf4_weight* W, const void* x, nf4_dtype xt, uint16_t* out,
+                                    nf4_stream stream);
+
+/*
  * Fused q/k/v projection, one launch over the three matrices' rows sharing x:
  *   q[m] = sum_k Wq_hat[m][k] * x[k] + bq[m]   (likewise k with Wk, bk and v with Wv, bv)
  * Source: same page, section 6 ("one grid over q.M+k.M+v.M rows sharing x (no

@@ -371,6 +371,17 @@ nf4_status nf4_gemv_swiglu(const nf4_weight* Wg, const nf4_weight* Wu, const voi
   return run_gemv(nf4k::EPI_SWIGLU, Wg, Wu, x, xt, nullptr, nullptr, out, nullptr, nullptr, stream, what);
 }
 
+nf4_status nf4_gemv_glu_interleaved(const nf4_weight* W, const void* x, nf4_dtype xt, uint16_t* out,
+                                    nf4_stream stream) {
+  const char* what = "nf4_gemv_glu_interleaved";
+  nf4_status st;
+  if ((st = check_weight(W, what)) || (st = check_x(x, xt, what)) || (st = check_out(out, 2, "out", what)))
+    return st;
+  if (W->M % 2 != 0)
+    return fail(NF4_EINVAL, "%s: W has %lld rows; interleaved gate/up rows come in pairs", what, (long long)W->M);
+  return run_gemv(nf4k::EPI_GLU, W, nullptr, x, xt, nullptr, nullptr, out, nullptr, nullptr, stream, what);
+}
+
 nf4_status nf4_gemv_argmax(const nf4_weight* W, const void* x, nf4_dtype xt, float* logits, int64_t* index,
                            void* workspace, nf4_stream stream) {
   const char* what = "nf4_gemv_argmax";

@@ -319,8 +319,18 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Epilogue kinds of the N=1 kernel.
-enum Epi : int { EPI_PLAIN = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3, EPI_QKV = 4 };
+// Epilogue kinds of the N=1 kernel.  EPI_GLU: one matrix whose rows alternate
+// gate and up (row 2c the gate, row 2c + 1 the up of output c), SwiGLU of
+// each pair.
+enum Epi : int { EPI_PLAIN = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3, EPI_QKV = 4, EPI_GLU = 5 };
+
+// First row of part p of n equal parts of M rows.  With interleaved gate/up
+// rows the split falls on even rows, so that an output's two rows stay in one
+// part (every kernel variant also keeps an even number of rows per group).
+template <int EPI>
+__host__ __device__ __forceinline__ int64_t part_first_row(int64_t p, int64_t n, int64_t M) {
+  return EPI == EPI_GLU ? 2 * (p * (M >> 1) / n) : p * M / n;
+}
 
 // Arguments of one N=1 launch.
 struct GemvArgs {

@@ -26,6 +26,7 @@ const void* kernel_ptr(int epi, int nch, int rb, bool big, bool xb) {
     case EPI_RESID: return GemvDispatch<EPI_RESID>::ptr(nch, rb, big, xb);
     case EPI_SWIGLU: return GemvDispatch<EPI_SWIGLU>::ptr(nch, rb, big, xb);
     case EPI_QKV: return GemvDispatch<EPI_QKV>::ptr(nch, rb, big, xb);
+    case EPI_GLU: return GemvDispatch<EPI_GLU>::ptr(nch, rb, big, xb);
     default: return GemvDispatch<EPI_ARGMAX>::ptr(nch, rb, big, xb);
   }
 }
@@ -64,6 +65,7 @@ const void* tma_ptr(int epi, int nch, int rb, int sub, bool xb, int lut) {
     case EPI_RESID: return GemvTmaDispatch<EPI_RESID>::ptr(nch, rb, sub, xb, lut);
     case EPI_SWIGLU: return GemvTmaDispatch<EPI_SWIGLU>::ptr(nch, rb, sub, xb, lut);
     case EPI_QKV: return GemvTmaDispatch<EPI_QKV>::ptr(nch, rb, sub, xb, lut);
+    case EPI_GLU: return GemvTmaDispatch<EPI_GLU>::ptr(nch, rb, sub, xb, lut);
     default: return GemvTmaDispatch<EPI_ARGMAX>::ptr(nch, rb, sub, xb, lut);
   }
 }
@@ -352,6 +354,8 @@ cudaError_t launch_gemv_tma(int epi, bool xb, const GemvArgs& a, const TmaConfig
       return GemvTmaDispatch<EPI_SWIGLU>::launch(c.nch, c.rb, c.sub, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
     case EPI_QKV:
       return GemvTmaDispatch<EPI_QKV>::launch(c.nch, c.rb, c.sub, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
+    case EPI_GLU:
+      return GemvTmaDispatch<EPI_GLU>::launch(c.nch, c.rb, c.sub, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
     default:
       return GemvTmaDispatch<EPI_ARGMAX>::launch(c.nch, c.rb, c.sub, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);
   }
@@ -364,6 +368,7 @@ cudaError_t launch_gemv(int epi, bool xb, const GemvArgs& a, GemvConfig cfg, cud
     case EPI_RESID: return GemvDispatch<EPI_RESID>::launch(cfg.nch, cfg.rb, cfg.big, xb, a, cfg, s);
     case EPI_SWIGLU: return GemvDispatch<EPI_SWIGLU>::launch(cfg.nch, cfg.rb, cfg.big, xb, a, cfg, s);
     case EPI_QKV: return GemvDispatch<EPI_QKV>::launch(cfg.nch, cfg.rb, cfg.big, xb, a, cfg, s);
+    case EPI_GLU: return GemvDispatch<EPI_GLU>::launch(cfg.nch, cfg.rb, cfg.big, xb, a, cfg, s);
     default: return GemvDispatch<EPI_ARGMAX>::launch(cfg.nch, cfg.rb, cfg.big, xb, a, cfg, s);
   }
 }

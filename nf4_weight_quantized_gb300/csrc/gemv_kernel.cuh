@@ -100,6 +100,7 @@ template <int NCH, int RB, int EPI, bool XBF16>
 __device__ __forceinline__ void gemv_body(const GemvArgs& a) {
   constexpr int NV = (EPI == EPI_SWIGLU) ? 2 : 1;  // matrices per row
   constexpr int P = Log2<RB>::value;
+  static_assert(EPI != EPI_GLU || RB % 2 == 0, "gate/up pairs need an even number of rows per batch");
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float cbs[16];
   __shared__ unsigned long long warp_keys[32];
@@ -114,8 +115,8 @@ __device__ __forceinline__ void gemv_body(const GemvArgs& a) {
   const int H = a.K >> 5;  // 16-byte chunks per row
   const int64_t NG = (int64_t)gridDim.x * a.gpc;
   const int64_t gg = (int64_t)blockIdx.x * a.gpc + group;
-  const int64_t r0 = gg * a.M / NG;
-  const int64_t r1 = (gg + 1) * a.M / NG;
+  const int64_t r0 = part_first_row<EPI>(gg, NG, a.M);
+  const int64_t r1 = part_first_row<EPI>(gg + 1, NG, a.M);
   const int64_t row_bytes = a.K >> 1;
   const int64_t nblk = a.K >> 6;
 
@@ -253,6 +254,11 @@ __device__ __forceinline__ void gemv_body(const GemvArgs& a) {
       }
       buf ^= 1;
     }
+    // interleaved gate/up: the up sum of an even (gate) row sits one row slot
+    // further on (32 / RB lanes after the transpose reduction, the next lane
+    // after the cross-warp sum); batches start on even rows
+    float up = 0.f;
+    if (EPI == EPI_GLU) up = __shfl_down_sync(0xffffffffu, v[0], WPG == 1 ? (32 >> P) : 1);
     if (row >= 0 && row < r1) {
       if (EPI == EPI_PLAIN) {
         a.y[row] = v[0];
@@ -265,6 +271,12 @@ __device__ __forceinline__ void gemv_body(const GemvArgs& a) {
         a.out_bf16[row] = __bfloat16_as_ushort(__float2bfloat16_rn(silu * u));
       } else if (EPI == EPI_QKV) {
         qkv_store(a, row, v[0]);
+      } else if (EPI == EPI_GLU) {
+        if (((row - rb0) & 1) == 0) {
+          const float g = v[0];
+          const float silu = g / (1.0f + expf(-g));
+          a.out_bf16[row >> 1] = __bfloat16_as_ushort(__float2bfloat16_rn(silu * up));
+        }
       } else {
         a.y[row] = v[0];
         const unsigned long long k = argmax_key(v[0], row);

@@ -92,6 +92,7 @@ __device__ __forceinline__ float chunk_dot_f16mix(const uint4 c, const uint32_t 
 template <int NCH, int RB, int SUB, int EPI, bool XBF16, int LUTM>
 __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid_constant__ TmaPlan P) {
   static_assert(SUB >= 1 && RB % SUB == 0, "SUB rows per full barrier must divide RB");
+  static_assert(EPI != EPI_GLU || RB % 2 == 0, "gate/up pairs need an even number of rows per group");
   constexpr int NV = (EPI == EPI_SWIGLU) ? 2 : 1;
   constexpr int PL = Log2<RB>::value;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -109,8 +110,8 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
   const int wig = t >> 5;
   const int WPG = G >> 5;
   const int H = a.K >> 5;
-  const int64_t R0 = (int64_t)blockIdx.x * a.M / gridDim.x;
-  const int64_t R1 = (int64_t)(blockIdx.x + 1) * a.M / gridDim.x;
+  const int64_t R0 = part_first_row<EPI>(blockIdx.x, gridDim.x, a.M);
+  const int64_t R1 = part_first_row<EPI>(blockIdx.x + 1, gridDim.x, a.M);
   const int n_it = (int)((R1 - R0 + P.SR - 1) / P.SR);
   const int row_bytes = a.K >> 1;
   const int nblk = a.K >> 6;
@@ -448,6 +449,11 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
         }
       }
       ++li;
+      // interleaved gate/up: the up sum of an even (gate) row sits one row
+      // slot further on, RB-row slots apart in lanes (32 / RB) after the
+      // transpose reduction, or in the next lane after the cross-warp sum
+      float up = 0.f;
+      if (EPI == EPI_GLU) up = __shfl_down_sync(0xffffffffu, v[0], WPG == 1 ? (32 >> PL) : 1);
       if (lr >= 0 && lr < rows && !*abort) {
         const int64_t row = rb + lr;
         if (EPI == EPI_PLAIN) {
@@ -461,6 +467,12 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
           a.out_bf16[row] = __bfloat16_as_ushort(__float2bfloat16_rn(silu * u));
         } else if (EPI == EPI_QKV) {
           qkv_store(a, row, v[0]);
+        } else if (EPI == EPI_GLU) {
+          if ((lr & 1) == 0) {  // stages and groups start on even rows
+            const float g = v[0];
+            const float silu = g / (1.0f + expf(-g));
+            a.out_bf16[row >> 1] = __bfloat16_as_ushort(__float2bfloat16_rn(silu * up));
+          }
         } else {
           a.y[row] = v[0];
           const unsigned long long k = argmax_key(v[0], row);

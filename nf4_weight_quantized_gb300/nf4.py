@@ -52,6 +52,7 @@ def _load():
         "nf4_gemv": [W, P, I, P, P],
         "nf4_gemv_residual": [W, P, I, P, P, P],
         "nf4_gemv_swiglu": [W, W, P, I, P, P],
+        "nf4_gemv_glu_interleaved": [W, P, I, P, P],
         "nf4_gemv_qkv": [W, W, W, P, P, P, P, I, P, P, P, P],
         "nf4_dequant_rows": [W, P, ctypes.c_int64, P, I, P],
         "nf4_gemv_argmax": [W, P, I, P, P, P, P],
@@ -81,7 +82,7 @@ lib = _load()
 EXPORTS = ("nf4_gemv", "nf4_gemv_residual", "nf4_gemv_swiglu", "nf4_gemv_argmax", "nf4_gemm_chunk",
            "nf4_workspace_bytes", "nf4_quantize", "nf4_codebook", "nf4_last_error", "nf4_describe_config",
            "nf4_check_device_errors", "nf4_gemm_chunk_noalloc", "nf4_gemv_qkv",
-           "nf4_dequant_rows")
+           "nf4_dequant_rows", "nf4_gemv_glu_interleaved")
 
 
 def _check(status: int):
@@ -175,6 +176,18 @@ def nf4_gemv_swiglu(Wg: NF4Weight, Wu: NF4Weight, x: torch.Tensor, out: torch.Te
     g, u = Wg.struct(), Wu.struct()
     _check(lib.nf4_gemv_swiglu(ctypes.byref(g), ctypes.byref(u), _dev(x, "x", numel=Wg.K), _xtype(x),
                                _dev(out, "out", torch.bfloat16, Wg.M), _stream(stream)))
+    return out
+
+
+def nf4_gemv_glu_interleaved(W: NF4Weight, x: torch.Tensor, out: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """SwiGLU over one matrix whose rows alternate gate (even) and up (odd):
+    out[c] = bf16(silu(v[2c]) * v[2c + 1]), v = W x; [W.M / 2] bf16."""
+    if out is None:
+        out = torch.empty(W.M // 2, dtype=torch.bfloat16, device=x.device)
+    w = W.struct()
+    _check(lib.nf4_gemv_glu_interleaved(ctypes.byref(w), _dev(x, "x", numel=W.K), _xtype(x),
+                                        _dev(out, "out", torch.bfloat16, W.M // 2), _stream(stream)))
     return out
 
 

@@ -83,7 +83,7 @@ def silu_product_bf16(seed: int, tid_a: int, tid_b: int, n: int) -> np.ndarray:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "gemv", "residual", "swiglu", "argmax", "chunk", "qkv", "embed"
+    kind: str  # "gemv", "residual", "swiglu", "argmax", "chunk", "qkv", "embed", "glu"
     M: int
     K: int
     N: int
@@ -100,6 +100,9 @@ WORKLOADS = {
                               "3B down_proj 2048x11008, x bf16 silu(z1)*z2, + fp32 residual"),
     "swiglu": Workload("swiglu", "swiglu", 11008, 2048, 1, 2, "bf16",
                        "3B gate/up 2x 11008x2048, x bf16 N(0,1), bf16 silu(g)*u out"),
+    "glu3b": Workload("glu3b", "glu", 11008, 2048, 1, 2, "bf16",
+                      "3B gate/up (the swiglu weights) interleaved into one 22016x2048 matrix, row 2c gate c, "
+                      "row 2c+1 up c, x bf16 N(0,1), bf16 silu(g)*u out"),
     "lm_head_argmax": Workload("lm_head_argmax", "argmax", 151936, 2048, 1, 3, "bf16",
                                "3B lm_head 151936x2048, x bf16 N(0,1), fp32 logits + argmax"),
     "chunk14b": Workload("chunk14b", "chunk", 13824, 5120, 32, 4, "bf16",
@@ -138,6 +141,11 @@ def workload_inputs(w: Workload, M: int | None = None) -> dict:
     elif w.kind == "swiglu":
         d["W"] = weights(s, 0, M, K)
         d["Wu"] = weights(s, 1, M, K)
+        d["x"] = normal_bf16(s, 2, K)
+    elif w.kind == "glu":  # M outputs: 2 M rows, gate and up alternating
+        d["W"] = np.empty((2 * M, K), np.float32)
+        d["W"][0::2] = weights(s, 0, M, K)
+        d["W"][1::2] = weights(s, 1, M, K)
         d["x"] = normal_bf16(s, 2, K)
     elif w.kind == "residual":
         d["W"] = weights(s, 0, M, K)

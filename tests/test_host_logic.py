@@ -61,6 +61,7 @@ def test_algorithmic_bytes():
     # codes K/2 + scales K/16 per row
     assert bench.bytes_of("residual", 2048, 11008)["total"] == 2048 * 11008 * 9 // 16 + 11008 * 2 + 2048 * 8
     assert bench.bytes_of("swiglu", 11008, 2048)["weight"] == 2 * 11008 * 2048 * 9 // 16
+    assert bench.bytes_of("glu", 11008, 2048) == bench.bytes_of("swiglu", 11008, 2048)
     assert bench.bytes_of("argmax", 151936, 2048)["total"] == 151936 * 2048 * 9 // 16 + 4096 + 151936 * 4 + 8
     assert bench.bytes_of("chunk", 13824, 5120, 32)["total"] == 13824 * 5120 * 9 // 16 + 32 * 5120 * 2 + 32 * 13824 * 4
     qkv = bench.bytes_of("qkv", 2048, 2048, 1, 256)
@@ -74,6 +75,10 @@ def test_workload_inputs_are_seeded():
     a, b = synth.workload_inputs(w), synth.workload_inputs(w)
     assert set(a) == {"W", "Wk", "Wv", "x", "bq", "bk", "bv"}
     assert all(np.array_equal(a[k], b[k]) for k in a)
+    # the interleaved gate/up workload holds the two-matrix SwiGLU weights
+    g, sw = synth.workload_inputs(synth.WORKLOADS["glu3b"], M=6), synth.workload_inputs(synth.WORKLOADS["swiglu"], M=6)
+    assert g["W"].shape == (12, 2048) and np.array_equal(g["x"], sw["x"])
+    assert np.array_equal(g["W"][0::2], sw["W"]) and np.array_equal(g["W"][1::2], sw["Wu"])
     ids = synth.token_ids(6, 1, 4096, 151936)
     assert ids.dtype == np.int64 and ids.min() >= 0 and ids.max() < 151936
     assert np.array_equal(ids, synth.token_ids(6, 1, 4096, 151936))
