@@ -193,8 +193,9 @@ int tma_groups_per_stage(int gpc, int G, int rb, int nv, int64_t K, const cudaFu
 // Bulk-copy kernel: x-stationary row groups as in the register kernel, plus a
 // producer warp and a ring of S stages of SR rows each, one block per SM.
 //
-// `pair`: size the block so that two fit on one SM (one row group, at most
-// half the SM's shared memory) and launch one per SM, so that the next call's
+// `pair`: size the block so that two fit on one SM (row groups whose
+// registers fill at most half the SM's register file, at most half its shared
+// memory) and launch one per SM, so that the next call's
 // block can enter beside this one and copy its first stages while this one
 // finishes its arithmetic (TmaPlan::early).
 static TmaConfig tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int device, bool pair) {
@@ -273,7 +274,16 @@ static TmaConfig tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int devi
       gpc = gpc < 1 ? 1 : (gpc > 14 ? 14 : gpc);
       while (gpc > 1 && gpc * c.G + 32 > attr.maxThreadsPerBlock) --gpc;
     } else {
-      gpc = pair ? 1 : pick_groups(c.G, c.rb, nv, M, K, attr, device);
+      gpc = pick_groups(c.G, c.rb, nv, M, K, attr, device);
+      if (pair && gpc >= 1) {
+        // at most the groups whose registers let two blocks share an SM
+        int regs_sm = 0;
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, device);
+        const int regs = attr.numRegs > 0 ? attr.numRegs : 255;
+        const int max_t = (regs_sm / (2 * regs)) / 32 * 32;
+        const int cap_g = (max_t - 32) / c.G;
+        gpc = gpc < cap_g ? gpc : cap_g;
+      }
     }
     if (gpc >= 1 && gpc * c.G + 32 <= attr.maxThreadsPerBlock) break;
     if (c.rb == 2 || attempt > 2) return c;
@@ -293,6 +303,14 @@ static TmaConfig tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int devi
   const int avail = limit - (int)attr.sharedSizeBytes - LUT_BYTES - red_set - 256;
   const int one_group = nv * c.rb * (row_bytes + srow_bytes);
   int gps = tma_groups_per_stage(gpc, c.G, c.rb, nv, K, attr, device);
+  if (pair) {  // the same rule within the paired budget
+    gps = 1;
+    for (int d = gpc; d >= 1; --d)
+      if (gpc % d == 0 && 2 * d * one_group <= avail) {
+        gps = d;
+        break;
+      }
+  }
   const int gps_env = env_int("NF4_TMA_GPS", 0);
   if (gps_env > 0 && gpc % gps_env == 0 && 2 * gps_env * one_group <= avail) gps = gps_env;
   c.GPS = gps;

@@ -79,3 +79,13 @@ def test_coresident_swiglu(nf4, M, K):
     out = nf4.nf4_gemv_swiglu(H.weight_tensors(gc, gs), H.weight_tensors(uc, us), H.x_tensor(x))
     of = synth.bf16_to_f32(H.bf16_bits_of(out)).astype(np.float64)
     assert np.all(np.abs(of - o64) <= H.swiglu_bound(g, u, Sg, Su) + H.ulp_bf16(o64))
+
+
+def test_coresident_keeps_several_groups_for_short_rows(nf4):
+    # K = 2048: a row group is one warp, so a paired block still holds several
+    import re
+
+    desc = nf4.nf4_describe_config(11008, 2048)
+    assert "two blocks per SM" in desc, desc
+    groups = int(re.search(r"(\d+) group\(s\)", desc).group(1))
+    assert groups >= 2, desc
