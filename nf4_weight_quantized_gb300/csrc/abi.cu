@@ -484,13 +484,10 @@ const char* nf4_describe_config(int64_t M, int64_t K, int N) {
       std::snprintf(buf, sizeof buf,
                     "gemv M=%lld K=%lld (16-byte aligned scales): bulk-copy kernel, %d thread(s) per row, %d row(s) "
                     "per group and stage, %d group(s) (%d per stage) + 1 producer warp per block (%d threads), %d stages of %d rows "
-                    "(%d B, %d row(s) per full barrier), %d blocks, %d B shared memory, %s table, %s%s",
+                    "(%d B, %d row(s) per full barrier), %d blocks, %d B shared memory, %s table, %s",
                     (long long)M, (long long)K, t.G, t.rb, t.gpc, t.GPS, t.threads, t.S, t.SR, t.stage_bytes, t.subr, t.blocks,
                     t.smem, t.lut == 1 ? "fp16-level mixed-precision loop for bf16 x" : "fp32 pair",
-                    nf4k::pdl_enabled() ? "programmatic dependent launch" : "plain launch",
-                    t.early ? ", sized for two blocks per SM (the next call's block copies its first stages before "
-                              "its dependency wait)"
-                            : "");
+                    nf4k::pdl_enabled() ? "programmatic dependent launch" : "plain launch");
     } else {
       const nf4k::GemvConfig c = nf4k::choose_gemv_config(nf4k::EPI_PLAIN, M, K, dev);
       std::snprintf(buf, sizeof buf,

@@ -401,7 +401,6 @@ struct TmaConfig {
   int SR, GPS, S, stage_bytes, codes_bytes, scales_bytes, bar_off, red_off;
   int sub;       // rows per full barrier within a group's rb rows (compiled variant)
   int subr, nb;  // rows per full barrier in the stage, full barriers per stage
-  int early;     // two blocks fit on an SM: copy the first stages before the dependency wait
 };
 TmaConfig choose_tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int device);
 

@@ -194,13 +194,13 @@ int tma_groups_per_stage(int gpc, int G, int rb, int nv, int64_t K, const cudaFu
 
 // Bulk-copy kernel: x-stationary row groups as in the register kernel, plus a
 // producer warp and a ring of S stages of SR rows each, one block per SM.
-//
-// `pair`: size the block so that two fit on one SM (row groups whose
-// registers fill at most half the SM's register file, at most half its shared
-// memory) and launch one per SM, so that the next call's
-// block can enter beside this one and copy its first stages while this one
-// finishes its arithmetic (TmaPlan::early).
-static TmaConfig tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int device, bool pair) {
+TmaConfig choose_tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int device) {
+  const int key_epi = 2 * epi + (x_bf16 ? 1 : 0);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_tma_cache.find(Key{key_epi, device, M, K});
+    if (it != g_tma_cache.end()) return it->second;
+  }
   TmaConfig c{};
   c.ok = false;
   const bool two = (epi == EPI_SWIGLU);
@@ -238,17 +238,6 @@ static TmaConfig tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int devi
     if (c.nch == 2 && M < 512LL * (sms > 0 ? sms : 1)) c.rb = 2;
   }
   c.rb = env_int("NF4_TMA_RB", c.rb);
-  // shared memory one block may hold when two share an SM
-  int pair_smem = 0;
-  if (pair) {
-    int per_sm = 0, reserved = 0;
-    cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
-    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, device);
-    pair_smem = per_sm / 2 - reserved;
-    // two stages beside the pair table, with 4 KB for barriers, reduction
-    // slots and static shared memory
-    while (c.rb > 2 && LUT_BYTES + 2 * nv * c.rb * (int)(K / 2 + K / 16) + 4096 > pair_smem) c.rb /= 2;
-  }
   // bf16 activations use the fp16-level mixed-precision loop unless NF4_LUT=0
   // asks for the exact fp32 table; fp32 activations always use the fp32 table
   c.lut = env_int("NF4_LUT", LUT_F16MIX) == LUT_F32 ? LUT_F32 : LUT_F16MIX;
@@ -277,15 +266,6 @@ static TmaConfig tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int devi
       while (gpc > 1 && gpc * c.G + 32 > attr.maxThreadsPerBlock) --gpc;
     } else {
       gpc = pick_groups(c.G, c.rb, nv, M, K, attr, device);
-      if (pair && gpc >= 1) {
-        // at most the groups whose registers let two blocks share an SM
-        int regs_sm = 0;
-        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, device);
-        const int regs = attr.numRegs > 0 ? attr.numRegs : 255;
-        const int max_t = (regs_sm / (2 * regs)) / 32 * 32;
-        const int cap_g = (max_t - 32) / c.G;
-        gpc = gpc < cap_g ? gpc : cap_g;
-      }
     }
     if (gpc >= 1 && gpc * c.G + 32 <= attr.maxThreadsPerBlock) break;
     if (c.rb == 2 || attempt > 2) return c;
@@ -301,18 +281,9 @@ static TmaConfig tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int devi
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   const int max_stages = 32;
-  const int limit = pair && pair_smem < optin ? pair_smem : optin;
-  const int avail = limit - (int)attr.sharedSizeBytes - LUT_BYTES - red_set - 256;
+  const int avail = optin - (int)attr.sharedSizeBytes - LUT_BYTES - red_set - 256;
   const int one_group = nv * c.rb * (row_bytes + srow_bytes);
   int gps = tma_groups_per_stage(gpc, c.G, c.rb, nv, K, attr, device);
-  if (pair) {  // the same rule within the paired budget
-    gps = 1;
-    for (int d = gpc; d >= 1; --d)
-      if (gpc % d == 0 && 2 * d * one_group <= avail) {
-        gps = d;
-        break;
-      }
-  }
   const int gps_env = env_int("NF4_TMA_GPS", 0);
   if (gps_env > 0 && gpc % gps_env == 0 && 2 * gps_env * one_group <= avail) gps = gps_env;
   c.GPS = gps;
@@ -355,46 +326,25 @@ static TmaConfig tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int devi
   c.red_off = (c.bar_off + bars_bytes * S + 15) / 16 * 16;
   c.smem = c.red_off + (S + 1) * red_set;
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, c.smem);
-  if (pair) cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   int sms = 0, bps = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, c.threads, c.smem);
-  if (bps < (pair ? 2 : 1)) {
+  if (bps < 1) {
     cudaGetLastError();
     return c;
   }
   const int64_t want = (M + c.SR - 1) / c.SR;
-  const int64_t have = (int64_t)sms * (pair ? 1 : bps);  // pair: the second slot is the next call's
+  const int64_t have = (int64_t)sms * bps;
   c.blocks = (int)(want < have ? want : have);
-  c.early = pair ? 1 : 0;
   c.ok = true;
   cudaGetLastError();
-  return c;
-}
-
-// NF4_TMA_CORESIDENT=1 asks for two blocks per SM (tma_config's `pair`) where
-// they fit, else the usual one-block configuration.
-TmaConfig choose_tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int device) {
-  const bool pair = env_int("NF4_TMA_CORESIDENT", 0) == 1;
-  const int key_epi = 4 * epi + (pair ? 2 : 0) + (x_bf16 ? 1 : 0);
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_tma_cache.find(Key{key_epi, device, M, K});
-    if (it != g_tma_cache.end()) return it->second;
-  }
-  TmaConfig c{};
-  if (pair) c = tma_config(epi, x_bf16, M, K, device, true);
-  if (!c.ok) c = tma_config(epi, x_bf16, M, K, device, false);
-  if (c.ok) {
-    std::lock_guard<std::mutex> lk(g_mu);
-    g_tma_cache[Key{key_epi, device, M, K}] = c;
-  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_tma_cache[Key{key_epi, device, M, K}] = c;
   return c;
 }
 
 cudaError_t launch_gemv_tma(int epi, bool xb, const GemvArgs& a, const TmaConfig& c, cudaStream_t s) {
-  TmaPlan p{c.SR, c.GPS, c.S, c.stage_bytes, c.codes_bytes, c.scales_bytes, c.bar_off, c.red_off, c.subr, c.nb,
-            c.early};
+  TmaPlan p{c.SR, c.GPS, c.S, c.stage_bytes, c.codes_bytes, c.scales_bytes, c.bar_off, c.red_off, c.subr, c.nb};
   switch (epi) {
     case EPI_PLAIN:
       return GemvTmaDispatch<EPI_PLAIN>::launch(c.nch, c.rb, c.sub, xb, xb ? c.lut : (int)LUT_F32, a, p, c.blocks, c.threads, c.smem, s);

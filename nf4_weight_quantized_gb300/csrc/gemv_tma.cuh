@@ -57,7 +57,6 @@ struct TmaPlan {
   int red_off;     // offset of the reduction buffers
   int SUBR;        // rows per full barrier: SUB, or SR (one per stage)
   int NB;          // full barriers per stage (SR / SUBR)
-  int early;       // copy the first S stages before the dependency wait
 };
 
 // Two mixed-precision FMAs: acc0 += lo(h) * lo(x), acc1 += hi(h) * hi(x),
@@ -210,17 +209,10 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
     }
   };
   // Before the previous kernel on the stream has finished (programmatic
-  // dependent launch) only shared memory and the weights are touched: the
-  // weights are never written by the kernel before (the library's calling
-  // convention), so they are prefetched into L2 or, when this block shares its
-  // SM with the previous kernel's block (P.early), copied into the first
-  // stages at once, overlapping that block's arithmetic tail.
+  // dependent launch) only shared memory and L2 prefetches are touched.
   pdl_launch_dependents();
   int issued = 0;
-  if (is_producer && lane == 0 && P.early) {
-    policy = policy_evict_first();
-    for (; issued < n_it && issued < P.S; ++issued) issue(issued);
-  } else if (is_producer && lane == 0) {
+  if (is_producer && lane == 0) {
     policy = policy_evict_first();
     for (int it = 0; it < n_it && it < P.S; ++it) {
       const int64_t rb = R0 + (int64_t)it * P.SR;
