@@ -48,6 +48,8 @@ def load():
     lib.nf4o_gemv_qkv.argtypes = [P, P, P, P, I64, P, I, P, I64, P, P]
     lib.nf4o_dequant_rows.argtypes = [P, P, I64, I64, P, I64, P, P, P]
     lib.nf4o_gemv_glu_interleaved.argtypes = [P, P, I64, I64, P, I, P, I64, P, P, P, P]
+    lib.nf4o_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double, P, P]
+    lib.nf4o_rmsnorm.restype = ctypes.c_int
     lib.nf4o_round_bf16.argtypes = [ctypes.c_double]
     lib.nf4o_round_bf16.restype = ctypes.c_uint16
     for name in ("nf4o_codebook", "nf4o_quantize", "nf4o_dequant", "nf4o_gemv", "nf4o_gemv_residual",
@@ -236,6 +238,24 @@ def gemm_chunk(codes, scales, X_bf16, rows=None):
     _check(load().nf4o_gemm_chunk(_ptr(codes), _ptr(scales), M, K, _ptr(X), N, _ptr(r), n, _ptr(Y),
                                   _ptr(S)), "gemm_chunk")
     return Y, S
+
+
+def rmsnorm(x, w_bf16, eps):
+    """RMSNorm of each row of x (fp32 [rows, K] or [K]) with bf16 gain bits
+    w [K]: (float64 y, float64 mean squares).  "Decode V2 -- resident
+    executor", section 3: x * rsqrt(mean(x^2) + eps) * w."""
+    x = np.ascontiguousarray(x, np.float32)
+    one = x.ndim == 1
+    if one:
+        x = x[None, :]
+    w = np.ascontiguousarray(w_bf16, np.uint16)
+    rows, K = x.shape
+    if w.shape != (K,):
+        raise ValueError("gain must have K elements")
+    y = np.zeros((rows, K), np.float64)
+    ms = np.zeros(rows, np.float64)
+    _check(load().nf4o_rmsnorm(_ptr(x), _ptr(w), rows, K, float(eps), _ptr(y), _ptr(ms)), "rmsnorm")
+    return (y[0], ms[0]) if one else (y, ms)
 
 
 def round_bf16(v: float) -> int:

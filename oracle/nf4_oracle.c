@@ -432,5 +432,31 @@ int nf4o_gemm_chunk(const uint8_t* codes, const float* scales, int64_t M, int64_
   return NF4O_OK;
 }
 
+/*
+ * RMSNorm of `rows` rows of K values: y[r][k] = x[r][k] * w[k] / sqrt(ms_r + eps),
+ * ms_r = (sum_k x[r][k]^2) / K.
+ * Source: "Decode V2 -- resident executor", section 3 "CPU oracle" (RMSNorm is
+ * x * rsqrt(mean(x^2) + eps) * w, Qwen-style, no bias) and section 2 (RMS
+ * weights are bf16 [hidden]); "golang.design/x/accel/tensor", func RMSNorm
+ * (each row normalized by its root mean square, scaled by a gain).
+ * x fp32 [rows][K], w bf16 bits [K]; everything in float64, k ascending.
+ * y_f64 (may be NULL) gets the float64 values, ms (may be NULL) the float64
+ * mean squares.
+ */
+int nf4o_rmsnorm(const float* x, const uint16_t* w, int64_t rows, int64_t K, double eps, double* y_f64,
+                 double* ms) {
+  if (!x || !w || rows < 1 || K < 1 || !(eps >= 0.0)) return NF4O_EINVAL;
+  for (int64_t r = 0; r < rows; ++r) {
+    double ss = 0.0;
+    for (int64_t k = 0; k < K; ++k) ss += (double)x[r * K + k] * (double)x[r * K + k];
+    const double m = ss / (double)K;
+    const double inv = 1.0 / sqrt(m + eps);
+    if (ms) ms[r] = m;
+    if (y_f64)
+      for (int64_t k = 0; k < K; ++k) y_f64[r * K + k] = (double)x[r * K + k] * inv * (double)bf16_bits_to_f32(w[k]);
+  }
+  return NF4O_OK;
+}
+
 /* Rounding helpers exposed for the tests: double -> bf16 bits (RN-even). */
 uint16_t nf4o_round_bf16(double v) { return f64_to_bf16_bits(v); }

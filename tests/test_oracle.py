@@ -16,6 +16,9 @@ SwiGLU with gate/up rows interleaved: a worked example using silu(0) = 0 and
 silu(z) - silu(-z) = z, and equality with the two-matrix SwiGLU.
 Chunk: equals the GEMV exactly when every W_hat is representable in bf16, and
 otherwise stays within the bf16 rounding bound of the weights.
+RMSNorm: closed forms (a row whose mean square is a perfect square, an eps that
+completes one, rows normalized separately), the bf16 gain bits, power-of-two
+scale invariance and unit root mean square of the output.
 """
 from __future__ import annotations
 
@@ -644,3 +647,58 @@ def test_glu_interleaved_rejects_bad_shapes(oracle_mod):
         oracle_mod.gemv_glu_interleaved(codes, scales, np.ones(K, np.float32))  # odd row count
     with pytest.raises(ValueError):
         oracle_mod.gemv_glu_interleaved(codes[:2], scales[:2], np.ones(K, np.float32), cols=[1])
+
+
+# ------------------------------------------------------------------ rmsnorm
+# "Decode V2 -- resident executor", section 3: x * rsqrt(mean(x^2) + eps) * w,
+# w bf16 [hidden]; "golang.design/x/accel/tensor", func RMSNorm: each row by
+# its own root mean square.
+
+BF16_ONE, BF16_TWO, BF16_MINUS_HALF, BF16_QUARTER = 0x3F80, 0x4000, 0xBF00, 0x3E80
+
+
+def test_rmsnorm_worked_example(oracle_mod):
+    # mean((1, 7, 1, 7)^2) = 100 / 4 = 25, so every value is divided by 5; a
+    # sum instead of a mean (10), sqrt instead of rsqrt, or a dropped gain fails
+    x = np.array([1.0, 7.0, 1.0, 7.0], np.float32)
+    w = np.array([BF16_ONE, BF16_TWO, BF16_MINUS_HALF, BF16_QUARTER], np.uint16)
+    y, ms = oracle_mod.rmsnorm(x, w, 0.0)
+    assert ms == 25.0
+    assert np.allclose(y, [0.2, 2.8, -0.1, 0.35], rtol=0, atol=1e-15)
+
+
+def test_rmsnorm_eps_inside_the_root(oracle_mod):
+    # mean square 1, eps 3: 1 / sqrt(1 + 3) = 1/2 exactly (eps dropped gives 1,
+    # eps added outside the root gives 1 / 1 + 3 = 4)
+    x = np.ones(8, np.float32)
+    w = np.full(8, BF16_TWO, np.uint16)
+    y, ms = oracle_mod.rmsnorm(x, w, 3.0)
+    assert ms == 1.0 and np.all(y == 1.0)
+
+
+def test_rmsnorm_rows_are_separate(oracle_mod):
+    x = np.array([[2.0, -2.0, 2.0, 2.0], [1.0, 7.0, 1.0, 7.0]], np.float32)
+    w = np.full(4, BF16_ONE, np.uint16)
+    y, ms = oracle_mod.rmsnorm(x, w, 0.0)
+    assert list(ms) == [4.0, 25.0]
+    assert np.all(y[0] == [1.0, -1.0, 1.0, 1.0])
+    assert np.allclose(y[1], [0.2, 1.4, 0.2, 1.4], rtol=0, atol=1e-15)
+
+
+def test_rmsnorm_scale_invariance_and_unit_rms(oracle_mod):
+    x = synth.normal_f32(77, 0, 3 * 2048).reshape(3, 2048)
+    w = np.full(2048, BF16_ONE, np.uint16)
+    y, _ = oracle_mod.rmsnorm(x, w, 0.0)
+    # with eps = 0 and a unit gain every row has root mean square 1
+    assert np.allclose(np.mean(y * y, axis=1), 1.0, rtol=0, atol=1e-12)
+    # power-of-two scaling of x is exact in fp32 and cancels
+    for e in (-20, -3, 5, 30):
+        y2, _ = oracle_mod.rmsnorm(x * np.float32(2.0 ** e), w, 0.0)
+        assert np.allclose(y2, y, rtol=1e-14, atol=0)
+
+
+def test_rmsnorm_rejects_bad_arguments(oracle_mod):
+    with pytest.raises(ValueError):
+        oracle_mod.rmsnorm(np.ones(4, np.float32), np.ones(3, np.uint16), 0.0)
+    with pytest.raises(ValueError):
+        oracle_mod.rmsnorm(np.ones(4, np.float32), np.ones(4, np.uint16), -1.0)
