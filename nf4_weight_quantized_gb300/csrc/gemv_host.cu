@@ -238,9 +238,9 @@ TmaConfig choose_tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int devi
     if (c.nch == 2 && M < 512LL * (sms > 0 ? sms : 1)) c.rb = 2;
   }
   c.rb = env_int("NF4_TMA_RB", c.rb);
-  // bf16 activations use the fp16-level mixed-precision loop unless NF4_LUT=0
-  // asks for the exact fp32 table; fp32 activations always use the fp32 table
-  c.lut = env_int("NF4_LUT", LUT_F16MIX) == LUT_F32 ? LUT_F32 : LUT_F16MIX;
+  // every activation dtype uses the exact fp32 levels; NF4_LUT=1 opts bf16
+  // activations into the narrower fp16-level mixed-precision loop
+  c.lut = env_int("NF4_LUT", LUT_F32) == LUT_F16MIX ? LUT_F16MIX : LUT_F32;
   auto lut_for = [&](int xb) { return xb ? c.lut : (int)LUT_F32; };
   // each activation dtype has its own instance and configuration (their
   // register use differs); when a row group does not fit in one block, retry

@@ -63,7 +63,11 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[RB], int lane) {
   return r;
 }
 
-// sum over the 32 weights of one 16-byte code chunk of cb[code] * x.
+// sum over the 32 weights of one 16-byte code chunk of cb[code] * x, exact
+// fp32 levels.  Per code byte: one PRMT (table address), one LDS.64 (both
+// levels) and two FFMAs.  (A packed fma.rn.f32x2 per byte issues fewer
+// instructions but measured slower inside the kernels: 53.5 against 49.3 us
+// on the 151936 x 2048 projection.)
 __device__ __forceinline__ float chunk_dot(const uint4 c, const float (&xv)[32], uint32_t laneoff,
                                            const uint8_t* lut) {
   float acc[4] = {0.f, 0.f, 0.f, 0.f};

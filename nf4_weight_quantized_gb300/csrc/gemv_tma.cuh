@@ -22,18 +22,20 @@
 //
 // Dequantization modes (LUTM):
 //  LUT_F32     pair table of exact fp32 levels: per code byte one PRMT, one
-//              conflict-free LDS.64, two FFMAs.  Bound by shared-memory
-//              bandwidth (8 bytes per two weights): about 26 weights per clock
-//              per SM.  Used for fp32 activations.
-//  LUT_F16MIX  pair table of fp16-rounded levels (relative error <= 2^-12 per
-//              level, well inside the stated 2e-3 bound): one LDS.32 per code
-//              byte halves the shared-memory traffic, and each weight costs one
-//              mixed-precision FMA (f16 x f16 -> f32 accumulate; the product is
-//              exact in fp32).  The thread's x slice is held as fp16 after
-//              scaling by a power of two that puts its largest magnitude in
-//              [2^14, 2^15): bf16 values convert exactly at any magnitude, and
-//              the scale is undone exactly with the block scale.  About 35
-//              weights per clock per SM.  Used for bf16 activations.
+//              conflict-free LDS.64 and one packed fma.rn.f32x2.  Bound by
+//              shared-memory bandwidth (8 bytes per two weights).  The default
+//              for every activation dtype.
+//  LUT_F16MIX  opt-in for bf16 activations (NF4_LUT=1): pair table of
+//              fp16-rounded levels (relative error up to 2^-12 per level):
+//              one LDS.32 per code byte halves the shared-memory traffic, and
+//              each weight costs one mixed-precision FMA (f16 x f16 -> f32
+//              accumulate; the product is exact in fp32).  The thread's x
+//              slice is held as fp16 after scaling by a power of two that puts
+//              its largest magnitude in [2^14, 2^15); the scale is undone
+//              exactly with the block scale.  A bf16 value converts exactly
+//              only while its scaled exponent is at least -17: values more
+//              than 2^31 below the slice's largest magnitude land in fp16
+//              subnormals and lose bits, or round to zero.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -372,7 +374,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
 #pragma unroll
       for (int sb = 0; sb < RB / SUB; ++sb) {
         const int lr0 = pos * RB + sb * SUB;
-        mbar_wait_bounded(full_bar(s, lr0 / P.SUBR), par, abort);
+        mbar_wait_bounded(full_bar(s, lr0 / P.SUBR), par, abort, a.wait_polls);
         uint4 c[NV][SUB][NCH];
         float scl[NV][SUB][NCH];
 #pragma unroll

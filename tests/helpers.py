@@ -82,5 +82,7 @@ def swiglu_bound(g, u, Sg, Su):
 
 
 def top2_gap(y: np.ndarray):
-    o = np.argsort(y)[::-1]
-    return float(y[o[0]] - y[o[1]]) if len(y) > 1 else math.inf
+    """Gap between the two largest DISTINCT values (rows that tie exactly are
+    one value: their order is fixed by the lowest-index rule)."""
+    u = np.unique(np.asarray(y, np.float64))
+    return float(u[-1] - u[-2]) if len(u) > 1 else math.inf

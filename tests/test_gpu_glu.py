@@ -102,7 +102,7 @@ def test_glu_interleaved_full_3b_gate_up(nf4):
     W[0::2], W[1::2] = d["W"], d["Wu"]
     codes, scales = oracle.quantize(W)
     ob, ref_bits = _check(nf4, H.weight_tensors(codes, scales), codes, scales, d["x"], "glu full 3B")
-    assert np.mean(ob == ref_bits) > 0.5
+    assert np.mean(ob == ref_bits) > 0.99  # fp32-accurate sums: nearly all round like the oracle
 
 
 def test_glu_interleaved_errors(nf4):
