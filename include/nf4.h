@@ -93,7 +93,14 @@ typedef enum nf4_dtype { NF4_F32 = 0, NF4_BF16 = 1 } nf4_dtype;
  *   W       weight (device codes/scales), shape M x K
  *   x       [K] activation, fp32 or bf16 (widened exactly to fp32)
  *   y       [M] fp32 output
- * Accumulation is fp32; |y - y_exact| <= 2e-3 * sum_k |x_k * W_hat[m][k]|.
+ * Dequantization uses the 16 levels as exact fp32 values: each level * x
+ * product is formed exactly inside a fused multiply-add, the block scale is
+ * applied once per 32 weights, and the sums are fp32;
+ * |y - y_exact| <= 2e-3 * sum_k |x_k * W_hat[m][k]|.
+ * (Opt-in, not the default: with the environment variable NF4_LUT=1, bf16 x
+ * takes a narrower loop with fp16-rounded levels, relative error up to 2^-12
+ * per level, in which x values more than 2^31 below the largest magnitude of
+ * their thread's 32- or 64-element slice lose bits or become zero.)
  * The result for a row depends only on that row's codes, scales and x (not on
  * its position), so identical rows give bit-identical outputs.
  */
@@ -183,6 +190,30 @@ nf4_status nf4_gemm_chunk(const nf4_weight* W, const uint16_t* X, int N, float* 
                           nf4_stream stream);
 
 /*
+ * RMSNorm of `rows` rows of K values, as its own small kernel ahead of a
+ * projection:  y[r][k] = x[r][k] * w[k] / sqrt(mean_k(x[r][k]^2) + eps)
+ * Source: "Decode V2 -- resident executor", section 3 (x * rsqrt(mean(x^2) +
+ * eps) * w, Qwen-style, no bias; RMS weights bf16 [hidden]), section 6 (RMS
+ * writes in place) and its status table (RMS fused into the following
+ * projections was a loss: every block repeats the reduction; RMS stays a
+ * one-block kernel); "golang.design/x/accel/tensor", func RMSNorm (each row by
+ * its own root mean square, computed in f32).
+ *   x     [rows][K] fp32, 4-byte aligned
+ *   w     [K] bf16 gain bits, 2-byte aligned
+ *   eps   finite, >= 0
+ *   y     [rows][K]: fp32 (yt = NF4_F32, 4-byte aligned; may be x itself, an
+ *         in-place update) or bf16 bits (yt = NF4_BF16, rounded to nearest
+ *         even; must not overlap x), ready as a projection's activation
+ * One block per row; the sum of squares is fp32 in a fixed order (the result
+ * depends only on the row), 1 / sqrt is IEEE-rounded.  Sizes: 1 <= K <=
+ * NF4_MAX_K, 1 <= rows < 2^31.  Like the projections, the kernel uses
+ * programmatic dependent launch: it lets the next kernel launch at once, and
+ * reads x only after the previous kernel has finished.
+ */
+nf4_status nf4_rmsnorm(const float* x, const uint16_t* w, int64_t rows, int64_t K, float eps, void* y,
+                       nf4_dtype yt, nf4_stream stream);
+
+/*
  * nf4_gemm_chunk without a caller workspace, for callers that cannot allocate
  * device memory: a host program that owns every allocation and hands this
  * library only its inputs and outputs, or a loop that must not call
@@ -195,7 +226,10 @@ nf4_status nf4_gemm_chunk(const nf4_weight* W, const uint16_t* X, int N, float* 
  *   and a message; use nf4_gemm_chunk for them.  (The 13824 x 5120 weight at
  *   N = 32 needs about 7.1 MB.)
  *   The first call on a device looks the array's device address up, with that
- *   device current; make it before any stream capture.  Every call on a device
+ *   device current; make it before any stream capture.  The address is kept
+ *   for the life of the process: after cudaDeviceReset, or anything else that
+ *   destroys and recreates the device's primary context, it is stale, and
+ *   this entry point must not be called again in that process.  Every call on a device
  *   shares the array: calls whose kernels may overlap on the GPU (different
  *   streams or host threads) race and must be serialized by the caller.  Each
  *   call clears the part of the scratch that must start at zero, then launches
@@ -246,6 +280,20 @@ nf4_status nf4_dequant_rows(const nf4_weight* E, const int64_t* ids, int64_t n, 
  * met an id outside its table, NF4_OK otherwise.
  */
 nf4_status nf4_check_device_errors(void);
+
+/*
+ * Diagnostic for failure-detection tests; never needed for correct results.
+ * Sets how many times the bulk-copy GEMV and the TMA prefill-chunk kernels
+ * poll for a stage of weights to land before giving up on it (0 restores the
+ * default, 2^22 polls).  With a limit of a few polls the first wait of a
+ * block usually runs out while its copies are still in flight: the block
+ * stops issuing copies, skips its remaining outputs, waits (with the full
+ * limit) for the copies it already issued, frees its tensor memory and sets
+ * the error word that nf4_check_device_errors() reports as NF4_ETIMEOUT.
+ * Outputs of such a call are invalid; workspaces are left zeroed as usual.
+ * Process-wide; applies to calls launched afterwards.
+ */
+void nf4_debug_set_wait_limit(uint32_t polls);
 
 /* Host copy of the 16 fp32 codebook levels the kernels use. Never fails. */
 void nf4_codebook(float out[16]);

@@ -2,6 +2,7 @@
 // configuration choice and asynchronous launches.  See include/nf4.h.
 #include <cmath>
 #include <cstdarg>
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -192,6 +193,7 @@ nf4_status run_gemv(int epi, const nf4_weight* W, const nf4_weight* W2, const vo
   a.M = (int)W->M;
   a.K = (int)W->K;
   a.cb = codebook();
+  a.wait_polls = nf4k::data_wait_polls();
   bool scales16_extra = true;
   if (qkv) {  // one row space: q's rows, then k's, then v's
     int64_t end = 0;
@@ -267,6 +269,15 @@ bool pdl_enabled() {
   return on;
 }
 
+namespace {
+std::atomic<uint32_t> g_data_wait_polls{0};  // 0: kWaitPolls
+}
+
+uint32_t data_wait_polls() {
+  const uint32_t v = g_data_wait_polls.load(std::memory_order_relaxed);
+  return v ? v : kWaitPolls;
+}
+
 thread_local std::string g_launch_note;
 
 void note_launch_failure(const void* fn, int threads, int smem, cudaError_t set_err, cudaError_t launch_err,
@@ -324,6 +335,8 @@ nf4_status nf4_check_device_errors(void) {
   return NF4_OK;
 }
 
+void nf4_debug_set_wait_limit(uint32_t polls) { nf4k::g_data_wait_polls.store(polls, std::memory_order_relaxed); }
+
 nf4_status nf4_dequant_rows(const nf4_weight* E, const int64_t* ids, int64_t n, void* out, nf4_dtype ot,
                             nf4_stream stream) {
   const char* what = "nf4_dequant_rows";
@@ -340,6 +353,25 @@ nf4_status nf4_dequant_rows(const nf4_weight* E, const int64_t* ids, int64_t n, 
                   what);
 }
 
+nf4_status nf4_rmsnorm(const float* x, const uint16_t* w, int64_t rows, int64_t K, float eps, void* y,
+                       nf4_dtype yt, nf4_stream stream) {
+  const char* what = "nf4_rmsnorm";
+  nf4_status st;
+  if (rows < 1 || rows >= (int64_t(1) << 31))
+    return fail(NF4_EINVAL, "%s: rows = %lld must be in [1, 2^31)", what, (long long)rows);
+  if (K < 1 || K > NF4_MAX_K) return fail(NF4_EINVAL, "%s: K = %lld must be in [1, %d]", what, (long long)K, NF4_MAX_K);
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(NF4_EINVAL, "%s: eps must be finite and >= 0", what);
+  if (yt != NF4_F32 && yt != NF4_BF16) return fail(NF4_EINVAL, "%s: output dtype %d is not NF4_F32 or NF4_BF16", what, (int)yt);
+  if ((st = check_out(x, 4, "x", what)) || (st = check_out(w, 2, "w", what)) ||
+      (st = check_out(y, yt == NF4_F32 ? 4 : 2, "y", what)))
+    return st;
+  if (yt == NF4_BF16 && static_cast<const void*>(y) == static_cast<const void*>(x))
+    return fail(NF4_EINVAL, "%s: a bf16 output cannot overwrite the fp32 input in place", what);
+  int dev = 0;
+  if ((st = current_device(&dev))) return st;
+  return launched(nf4k::launch_rmsnorm(x, w, rows, K, eps, y, yt == NF4_BF16, reinterpret_cast<cudaStream_t>(stream)),
+                  what);
+}
 
 nf4_status nf4_gemv(const nf4_weight* W, const void* x, nf4_dtype xt, float* y, nf4_stream stream) {
   const char* what = "nf4_gemv";

@@ -13,6 +13,9 @@
 // code must never hand it to a kernel.  Its device address is looked up once
 // per device with cudaGetSymbolAddress (with that device current) on the first
 // call made on that device; make that first call before any stream capture.
+// The address is cached for the life of the process, so it goes stale if the
+// device's primary context is destroyed and recreated (cudaDeviceReset): the
+// entry point must not be used again in such a process.
 // Every call on a device shares the one array and leaves its last contents in
 // it, so calls whose kernels overlap on the GPU (other streams, other host
 // threads) race on it.  The part that must start at zero (the per-tile

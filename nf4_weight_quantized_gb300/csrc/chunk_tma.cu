@@ -97,6 +97,7 @@ struct StreamKArgs {
   long long U;            // units = tiles * NQ
   int B;                  // blocks
   int maxseg;             // partial slots per tile (0: whole tiles per block)
+  uint32_t wait_polls;    // limit of the dequantizing warps' waits for staged units
 };
 
 // First unit of block b: an equal share of the units, or, when there are at
@@ -158,9 +159,10 @@ __device__ __forceinline__ void mul2_f32(float& r0, float& r1, float a0, float a
 
 // Bounded wait that sleeps `ns` nanoseconds between polls (waits that are long
 // by design leave the barrier unit to the threads on the critical path).
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t ns) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t ns,
+                                                uint32_t polls = kWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i) {
+    if (polls == kWaitPolls ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity)) return true;
     if (*abort) return false;
     if (ns) __nanosleep(ns);
   }
@@ -173,9 +175,9 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, v
 // orders their later accesses after the phase lane 0 observed (one poller per
 // warp instead of 32).
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort, int lane,
-                                               uint32_t ns) {
+                                               uint32_t ns, uint32_t polls = kWaitPolls) {
   int ok = 1;
-  if (lane == 0) ok = mbar_wait_sleep(bar, parity, abort, ns) ? 1 : 0;
+  if (lane == 0) ok = mbar_wait_sleep(bar, parity, abort, ns, polls) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int j = 0;
     for (int q = 0; q < nq; ++q) {
       const int s = q % SR;
-      mbar_wait_warp(raw_full(s), (uint32_t)((q / SR) & 1), abort, lane, NF4_DQ_SLEEP);
+      mbar_wait_warp(raw_full(s), (uint32_t)((q / SR) & 1), abort, lane, NF4_DQ_SLEEP, a.wait_polls);
       const uint8_t* raw = raw0 + s * RAW_BYTES;
       const float4 sc4 = *reinterpret_cast<const float4*>(raw + CODES_BYTES + KQ * XT_BYTES + r * 16);
       const float scl[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
@@ -571,6 +573,7 @@ cudaError_t launch_chunk_tma(const uint8_t* codes, const float* scales, int M, i
   a.U = p.U;
   a.B = p.B;
   a.maxseg = p.maxseg;
+  a.wait_polls = data_wait_polls();
   return checked_launch(reinterpret_cast<const void*>(&chunk_tma_kernel), NTHREADS, SMEM_BYTES, [&] {
     chunk_tma_kernel<<<p.B, NTHREADS, SMEM_BYTES, s>>>(mc, ms, mx, a, cb);
   });

@@ -76,6 +76,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of one barrier phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Upper bound on polls of one barrier phase (each poll may itself block for a
 // short hardware-defined time); past it the kernel gives up (see WaitGuard).
 constexpr uint32_t kWaitPolls = 1u << 22;
@@ -114,9 +127,13 @@ const DeviceErrorRegistration g_device_error_registration;
 // Bounded wait on one barrier phase.  `abort` is a block-shared flag: once any
 // wait in the block has timed out, later waits return at once, so the block
 // runs to its end (keeping every block-level barrier matched) without hanging.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+// `polls` is the limit (kWaitPolls unless a failure-detection test shortened
+// the waits for data to arrive, see data_wait_polls; a shortened wait polls
+// without suspending, so its limit is a count of tests, not of time slices).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  uint32_t polls = kWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i) {
+    if (polls == kWaitPolls ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity)) return true;
     if (*abort) return false;
   }
   *abort = 1;
@@ -163,6 +180,11 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
 // Host: programmatic dependent launch for the streaming kernels (NF4_PDL=0
 // turns it off).
 bool pdl_enabled();
+
+// Host: poll limit of the kernels' waits for their weight data to arrive
+// (kWaitPolls unless nf4_debug_set_wait_limit set another).  Waits that drain
+// copies already in flight always keep kWaitPolls.
+uint32_t data_wait_polls();
 
 __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
@@ -348,6 +370,7 @@ struct GemvArgs {
   int K;
   int G;    // threads cooperating on one row (multiple of 32)
   int gpc;  // row groups per block
+  uint32_t wait_polls;  // limit of the waits for staged weights (data_wait_polls)
   Codebook cb;
   // fused q/k/v (EPI_QKV): one row space over three matrices sharing x; rows
   // [0, seg_end[0]) are matrix 0's, [seg_end[0], seg_end[1]) matrix 1's,
@@ -420,6 +443,10 @@ cudaError_t launch_gemv(int epi, bool x_bf16, const GemvArgs& a, GemvConfig cfg,
 GemvConfig choose_gemv_config(int epi, int64_t M, int64_t K, int device);
 cudaError_t launch_quantize(const float* W, int64_t M, int64_t K, uint8_t* codes, float* scales,
                             const Codebook& cb, cudaStream_t s, int device);
+
+// RMSNorm, one block per row (rmsnorm.cu).
+cudaError_t launch_rmsnorm(const float* x, const uint16_t* w, int64_t rows, int64_t K, float eps, void* y,
+                           bool y_bf16, cudaStream_t s);
 
 // Prefill chunk (chunk.cu).
 cudaError_t launch_embed_rows(const uint8_t* codes, const float* scales, int64_t V, int64_t K, const int64_t* ids,

@@ -59,6 +59,7 @@ def _load():
         "nf4_gemm_chunk": [W, P, I, P, P, P],
         "nf4_gemm_chunk_noalloc": [W, P, I, P, P],
         "nf4_quantize": [P, ctypes.c_int64, ctypes.c_int64, P, P, P],
+        "nf4_rmsnorm": [P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, P, I, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -74,6 +75,8 @@ def _load():
     lib.nf4_describe_config.restype = ctypes.c_char_p
     lib.nf4_check_device_errors.argtypes = []
     lib.nf4_check_device_errors.restype = ctypes.c_int
+    lib.nf4_debug_set_wait_limit.argtypes = [ctypes.c_uint32]
+    lib.nf4_debug_set_wait_limit.restype = None
     return lib
 
 
@@ -82,7 +85,7 @@ lib = _load()
 EXPORTS = ("nf4_gemv", "nf4_gemv_residual", "nf4_gemv_swiglu", "nf4_gemv_argmax", "nf4_gemm_chunk",
            "nf4_workspace_bytes", "nf4_quantize", "nf4_codebook", "nf4_last_error", "nf4_describe_config",
            "nf4_check_device_errors", "nf4_gemm_chunk_noalloc", "nf4_gemv_qkv",
-           "nf4_dequant_rows", "nf4_gemv_glu_interleaved")
+           "nf4_dequant_rows", "nf4_gemv_glu_interleaved", "nf4_debug_set_wait_limit", "nf4_rmsnorm")
 
 
 def _check(status: int):
@@ -222,6 +225,21 @@ def nf4_dequant_rows(E: NF4Weight, ids: torch.Tensor, out: torch.Tensor | None =
     return out
 
 
+def nf4_rmsnorm(x: torch.Tensor, w: torch.Tensor, eps: float, out: torch.Tensor | None = None,
+                dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """RMSNorm of each row of x (fp32 [K] or [rows, K]) with bf16 gain w [K]:
+    x * w / sqrt(mean(x^2) + eps), fp32 or bf16; `out` may be x itself (fp32)."""
+    if x.dim() not in (1, 2):
+        raise ValueError("x must be [K] or [rows, K]")
+    K = x.shape[-1]
+    rows = 1 if x.dim() == 1 else x.shape[0]
+    if out is None:
+        out = torch.empty(x.shape, dtype=dtype, device=x.device)
+    _check(lib.nf4_rmsnorm(_dev(x, "x", torch.float32), _dev(w, "w", torch.bfloat16, K), rows, K, float(eps),
+                           _dev(out, "out", out.dtype, rows * K), _xtype(out), _stream(stream)))
+    return out
+
+
 def nf4_workspace_bytes(M: int, K: int, N: int = 1) -> int:
     return int(lib.nf4_workspace_bytes(M, K, N))
 
@@ -292,6 +310,12 @@ def nf4_check_device_errors() -> None:
     """Synchronize; raise NF4Error(NF4_ETIMEOUT) if a kernel's bounded wait ran out, or
     NF4Error(NF4_ERANGE) if nf4_dequant_rows met an id outside its table."""
     _check(lib.nf4_check_device_errors())
+
+
+def nf4_debug_set_wait_limit(polls: int) -> None:
+    """Failure-detection tests only: poll limit of the kernels' waits for staged
+    weights (0 restores the default)."""
+    lib.nf4_debug_set_wait_limit(int(polls))
 
 
 def nf4_last_error() -> str:
