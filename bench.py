@@ -435,6 +435,34 @@ def run_gpu(args, rank, world, dist):
            "h2d_bytes_per_step": x_host.numel() * 2 + r_host.numel() * 4,
            "d2h_bytes_per_step": y_host.numel() * 4, "steps": n_e2e,
            "us_per_step": e2e_secs / n_e2e * 1e6}
+    # the same step recorded once per weight copy as a CUDA graph (host -> device
+    # copies, the call, device -> host copy) and replayed: how a decode loop
+    # issues it, without the per-call Python work
+    graphs = []
+    for i in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            x_dev.copy_(x_host, non_blocking=True)
+            r_dev.copy_(r_host, non_blocking=True)
+            nf4.nf4_gemv_residual(Ws[i], x_dev, r_dev, y_dev)
+            y_host.copy_(y_dev, non_blocking=True)
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % copies].replay()
+    stream.synchronize()
+    if dist is not None:
+        dist.barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(n_e2e):
+            graphs[i % copies].replay()
+        e1.record(stream)
+    stream.synchronize()
+    g_secs = reduce_max(dist, e0.elapsed_time(e1) / 1e3, device)
+    e2e["graph"] = {"value": replica_value(world, b["weight"], n_e2e, g_secs), "unit": UNIT,
+                    "us_per_step": g_secs / n_e2e * 1e6, "steps": n_e2e}
+    del graphs
     del ctx, Ws
     torch.cuda.empty_cache()
 
