@@ -13,14 +13,20 @@ from CUDA graphs on one stream and timed with CUDA events on that stream,
 after W warm-up calls, bracketed by a barrier and a device synchronize.
 ``e2e`` repeats the measurement through the public Python API with the step's
 activation and residual copied from pinned host memory and its output copied
-back inside the timed region (weights stay resident, as in decode).
+back inside the timed region (weights stay resident, as in decode): the step
+recorded as a CUDA graph and replayed (how a decode loop issues it), with the
+eager Python loop's figure beside it.
 
+``cpu_baseline`` times the oracle on the host: one thread, and one spawned
+process per core over disjoint row ranges (the all-core figure).
 ``--impl reference`` times the CPU oracle instead (the reference arm of this
 repository; it is deliberately slow, plain C, single-threaded).
 
-Other workloads (SwiGLU, lm_head + argmax, 14B N=1, 14B chunk, fused 3B q/k/v, embedding-row
-gather of a 4096-token prompt) are reported
-under "workloads" with the same method and fewer calls.
+Other workloads (SwiGLU, interleaved gate/up SwiGLU, lm_head + argmax, 14B N=1,
+14B chunk, fused 3B q/k/v, embedding-row gather of a 4096-token prompt,
+RMSNorm of a decode step and of a prefill chunk) are reported compactly under
+"workloads" with the same method and fewer calls; ``--describe`` prints their
+launch configurations.
 """
 from __future__ import annotations
 
@@ -40,6 +46,9 @@ sys.path.insert(0, ROOT)
 METRIC = "NF4 GEMV effective weight GB/s (N=1, 3B down_proj 2048x11008 + residual)"
 UNIT = "GB/s"
 MAIN = "down_residual"
+# reported beside the main workload, in this order
+WORKLOADS = ("swiglu", "glu3b", "lm_head_argmax", "gemv14b", "chunk14b", "qkv3b", "embed_prefill", "rmsnorm3b",
+             "rmsnorm_chunk14b")
 WORKLOAD_NAME = "3B down_proj 2048x11008 NF4 (block 64, fp32 scales) + fp32 residual, x bf16, N=1"
 
 
@@ -127,6 +136,8 @@ class ClockSampler:
 
 def bytes_of(kind: str, M: int, K: int, N: int = 1, M_kv: int = 0) -> dict:
     """Algorithmic bytes per call: weight (codes + scales) and total."""
+    if kind == "rmsnorm":  # M rows of K: read fp32 rows and the bf16 gain, write bf16 rows
+        return {"weight": K * 2, "total": M * K * 4 + K * 2 + M * K * 2}
     if kind == "embed":  # N gathered rows of an M-row table: read N rows, write N bf16 rows
         w = N * (K // 2 + (K // 64) * 4)
         return {"weight": w, "total": w + N * 8 + N * K * 2, "table": M * K // 2 + M * (K // 64) * 4}
@@ -154,6 +165,8 @@ def describe(nf4, w) -> str:
     if w.kind == "embed":
         return (f"nf4_dequant_rows: {w.N} rows of a {w.M}x{w.K} NF4 table, bf16 out, one thread per 32 weights, "
                 "256-thread blocks")
+    if w.kind == "rmsnorm":
+        return f"nf4_rmsnorm: {w.M} row(s) of {w.K}, one block per row, bf16 out"
     rows = 2 * w.M if w.kind == "glu" else w.M + 2 * w.M_kv
     return nf4.nf4_describe_config(rows, w.K, w.N)
 
@@ -186,6 +199,13 @@ def build_calls(name: str, torch, nf4, synth, device, copies=None):
     def bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
 
+    if w.kind == "rmsnorm":  # no weights: inputs are tiny and stay in L2, as in a decode step
+        copies = 1
+        x = torch.from_numpy(d["x"]).to(device)
+        g = bf16(d["w"])
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+        call = lambda i, s: nf4.nf4_rmsnorm(x, g, 1e-6, out, stream=s)
+        return call, copies, b, {"x": x, "w": g, "out": out}
     if w.kind == "residual":
         Ws = replicate(quant(d["W"]))
         x = bf16(d["x"])
@@ -297,9 +317,34 @@ def time_calls(torch, call, copies: int, steps: int, warmup: int, stream, dist=N
 
 # ------------------------------------------------------------- CPU baseline
 
+def _oracle_rows_worker(task):
+    """One host process of the all-core oracle timing: the oracle as it stands
+    (single-threaded C) on its own contiguous range of the workload's rows,
+    repeated until the deadline; returns (calls, seconds)."""
+    codes, scales, x, r, r0, r1, target_s = task
+    import oracle
+
+    rows = np.arange(r0, r1)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.gemv_residual(codes, scales, x, r, rows=rows)
+        n += 1
+        if time.perf_counter() - t0 >= target_s:
+            break
+    return n, time.perf_counter() - t0
+
+
 def cpu_oracle_run(target_s: float):
-    """The oracle on the host, single-threaded, on the main workload: repeat
-    full down_proj + residual calls until target_s has elapsed."""
+    """The oracle on the host's cores, on the main workload.
+
+    Single thread: full down_proj + residual calls repeated for target_s.
+    All cores: one spawned process per core, each running the same oracle on
+    its own contiguous share of the rows for target_s; a full call takes as
+    long as the slowest share, so the value is weight bytes x calls of the
+    slowest process / its time."""
+    import multiprocessing as mp
+
     import oracle
     from nf4_weight_quantized_gb300 import synth
 
@@ -315,9 +360,21 @@ def cpu_oracle_run(target_s: float):
         if time.perf_counter() - t0 >= target_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": b["weight"] * n / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"full down_proj 2048x11008 + residual, {n} call(s), {dt:.1f} s, 1 thread",
-            "us_per_call": dt / n * 1e6}
+    single = {"value": b["weight"] * n / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+              "sample": f"full down_proj 2048x11008 + residual, {n} call(s), {dt:.1f} s, 1 thread",
+              "us_per_call": dt / n * 1e6}
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    if cores < 2:
+        return single
+    bounds = [w.M * i // cores for i in range(cores + 1)]
+    tasks = [(codes, scales, d["x"], d["r"], bounds[i], bounds[i + 1], target_s) for i in range(cores)]
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.map(_oracle_rows_worker, tasks)
+    per_call = max(t / c for c, t in res)
+    return {"value": b["weight"] / per_call / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"full down_proj 2048x11008 + residual, rows split over {cores} spawned processes "
+                       f"(one per core), {min(c for c, _ in res)}+ call(s) each in {target_s:.0f} s"),
+            "us_per_call": per_call * 1e6, "single_thread": single}
 
 
 def run_reference(args, rank, world):
@@ -431,10 +488,8 @@ def run_gpu(args, rank, world, dist):
     stream.synchronize()
     e2e_secs = e0.elapsed_time(e1) / 1e3
     e2e_secs = reduce_max(dist, e2e_secs, device)
-    e2e = {"value": replica_value(world, b["weight"], n_e2e, e2e_secs), "unit": UNIT,
-           "h2d_bytes_per_step": x_host.numel() * 2 + r_host.numel() * 4,
-           "d2h_bytes_per_step": y_host.numel() * 4, "steps": n_e2e,
-           "us_per_step": e2e_secs / n_e2e * 1e6}
+    eager = {"value": replica_value(world, b["weight"], n_e2e, e2e_secs), "unit": UNIT,
+             "us_per_step": e2e_secs / n_e2e * 1e6, "steps": n_e2e}
     # the same step recorded once per weight copy as a CUDA graph (host -> device
     # copies, the call, device -> host copy) and replayed: how a decode loop
     # issues it, without the per-call Python work
@@ -460,30 +515,35 @@ def run_gpu(args, rank, world, dist):
         e1.record(stream)
     stream.synchronize()
     g_secs = reduce_max(dist, e0.elapsed_time(e1) / 1e3, device)
-    e2e["graph"] = {"value": replica_value(world, b["weight"], n_e2e, g_secs), "unit": UNIT,
-                    "us_per_step": g_secs / n_e2e * 1e6, "steps": n_e2e}
+    # headline: the graph form (how a decode loop issues its step); the
+    # eager Python loop's figure is kept beside it
+    e2e = {"value": replica_value(world, b["weight"], n_e2e, g_secs), "unit": UNIT,
+           "h2d_bytes_per_step": x_host.numel() * 2 + r_host.numel() * 4,
+           "d2h_bytes_per_step": y_host.numel() * 4, "steps": n_e2e,
+           "us_per_step": g_secs / n_e2e * 1e6,
+           "form": "step (2 pinned H2D copies, nf4_gemv_residual, 1 D2H copy) recorded as a CUDA graph, replayed",
+           "eager": eager}
     del graphs
     del ctx, Ws
     torch.cuda.empty_cache()
 
+    # other workloads, compact (us per call, algorithmic GB/s, fraction of the
+    # measured HBM peak) so the whole line stays short; their launch
+    # configurations are printed by `python bench.py --describe`
     workloads = {}
     if args.all_workloads:
-        for name in ("swiglu", "glu3b", "lm_head_argmax", "gemv14b", "chunk14b", "qkv3b", "embed_prefill"):
+        for name in WORKLOADS:
             try:
                 c2, cp2, b2, ctx2 = build_calls(name, torch, nf4, synth, device)
                 n2 = args.workload_steps
                 s2, _ = time_calls(torch, c2, cp2, n2, args.warmup, stream, dist)
                 pc = s2 / n2
-                workloads[name] = {
-                    "us_per_call": pc * 1e6, "weight_gbs": b2["weight"] / pc / 1e9,
-                    "algorithmic_gbs": b2["total"] / pc / 1e9,
-                    "frac_of_hbm": b2["total"] / pc / 1e9 / peaks["hbm_gbs"],
-                    "algorithmic_bytes": b2["total"], "traffic": ncu_traffic(name), "copies": cp2, "calls": n2,
-                    "config": describe(nf4, synth.WORKLOADS[name])}
+                workloads[name] = {"us": round(pc * 1e6, 3), "gbs": round(b2["total"] / pc / 1e9, 1),
+                                   "frac": round(b2["total"] / pc / 1e9 / peaks["hbm_gbs"], 4)}
                 del ctx2, c2
                 torch.cuda.empty_cache()
             except Exception as e:  # report, keep the main line
-                workloads[name] = {"error": f"{type(e).__name__}: {e}"}
+                workloads[name] = {"error": f"{type(e).__name__}: {e}"[:200]}
 
     if rank != 0:
         return
@@ -541,9 +601,19 @@ def main():
     ap.add_argument("--no-workloads", dest="all_workloads", action="store_false")
     ap.add_argument("--ncu", default=None, help="run a few untimed calls of one workload (for ncu) and exit")
     ap.add_argument("--ncu-calls", type=int, default=3)
+    ap.add_argument("--describe", action="store_true", help="print each workload's launch configuration and exit")
     args = ap.parse_args()
     if args.ncu:
         run_profile_target(args.ncu, args.ncu_calls)
+        return
+    if args.describe:
+        from nf4_weight_quantized_gb300 import nf4, synth
+
+        for name in (MAIN,) + WORKLOADS:
+            w = synth.WORKLOADS[name]
+            b = bytes_of(w.kind, w.M, w.K, w.N, w.M_kv)
+            print(json.dumps({"workload": name, "description": w.description, "algorithmic_bytes": b["total"],
+                              "config": describe(nf4, w)}))
         return
     if args.warmup < 3:
         args.warmup = 3

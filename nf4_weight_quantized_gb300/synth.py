@@ -83,7 +83,7 @@ def silu_product_bf16(seed: int, tid_a: int, tid_b: int, n: int) -> np.ndarray:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "gemv", "residual", "swiglu", "argmax", "chunk", "qkv", "embed", "glu"
+    kind: str  # "gemv", "residual", "swiglu", "argmax", "chunk", "qkv", "embed", "glu", "rmsnorm"
     M: int
     K: int
     N: int
@@ -114,6 +114,11 @@ WORKLOADS = {
                       M_kv=256),
     "embed_prefill": Workload("embed_prefill", "embed", 151936, 2048, 4096, 6, "bf16",
                               "3B embedding table 151936x2048 kept as NF4, 4096 token ids uniform, bf16 rows out"),
+    "rmsnorm3b": Workload("rmsnorm3b", "rmsnorm", 1, 2048, 1, 7, "bf16",
+                          "3B decode RMSNorm: x fp32 [2048] N(0,1), bf16 gain 1 + 0.25 N(0,1), eps 1e-6, bf16 out"),
+    "rmsnorm_chunk14b": Workload("rmsnorm_chunk14b", "rmsnorm", 32, 5120, 32, 8, "bf16",
+                                 "14B prefill-chunk RMSNorm: x fp32 [32][5120] N(0,1), bf16 gain, eps 1e-6, "
+                                 "bf16 out"),
 }
 
 
@@ -151,6 +156,9 @@ def workload_inputs(w: Workload, M: int | None = None) -> dict:
         d["W"] = weights(s, 0, M, K)
         d["x"] = silu_product_bf16(s, 1, 2, K)
         d["r"] = normal_f32(s, 3, M)
+    elif w.kind == "rmsnorm":  # M rows of K
+        d["x"] = normal_f32(s, 0, M * K).reshape(M, K)
+        d["w"] = f32_bits_to_bf16((1.0 + 0.25 * normal_f32(s, 1, K)).astype(np.float32))
     elif w.kind in ("chunk",) or w.name == "gemv14b":
         d["W"] = weights(s, 0, M, K)
         X = normal_bf16(s, 1, 32 * K).reshape(32, K)

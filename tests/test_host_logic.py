@@ -68,6 +68,28 @@ def test_algorithmic_bytes():
     assert qkv["weight"] == 2560 * 2048 * 9 // 16 and qkv["total"] == qkv["weight"] + 4096 + 2560 * 8
     e = bench.bytes_of("embed", 151936, 2048, 4096)
     assert e["weight"] == 4096 * 1152 and e["total"] == 4096 * 1152 + 4096 * 8 + 4096 * 2048 * 2
+    # RMSNorm: fp32 rows in, bf16 gain, bf16 rows out
+    assert bench.bytes_of("rmsnorm", 32, 5120, 32)["total"] == 32 * 5120 * 6 + 5120 * 2
+
+
+def test_every_reported_workload_is_defined():
+    for name in bench.WORKLOADS:
+        w = synth.WORKLOADS[name]
+        d = synth.workload_inputs(w, M=min(w.M, 4)) if w.kind != "rmsnorm" else synth.workload_inputs(w)
+        assert d
+    r = synth.workload_inputs(synth.WORKLOADS["rmsnorm_chunk14b"])
+    assert r["x"].shape == (32, 5120) and r["x"].dtype == np.float32 and r["w"].dtype == np.uint16
+
+
+def test_all_core_oracle_worker_covers_its_rows():
+    # one share of the all-core CPU baseline: the oracle on rows [r0, r1)
+    import oracle
+
+    codes, scales = oracle.quantize(synth.weights(90, 0, 64, 256))
+    x = synth.normal_bf16(90, 1, 256)
+    r = synth.normal_f32(90, 2, 64)
+    n, secs = bench._oracle_rows_worker((codes, scales, x, r, 16, 48, 0.01))
+    assert n >= 1 and secs > 0
 
 
 def test_workload_inputs_are_seeded():
