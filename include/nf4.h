@@ -284,8 +284,9 @@ nf4_status nf4_check_device_errors(void);
 /*
  * Diagnostic for failure-detection tests; never needed for correct results.
  * Sets how many times the bulk-copy GEMV and the TMA prefill-chunk kernels
- * poll for a stage of weights to land before giving up on it (0 restores the
- * default, 2^22 polls).  With a limit of a few polls the first wait of a
+ * poll for their staged weights (and, in the chunk, for the dequantized
+ * operand the tensor core reads) before giving up (0 restores the default,
+ * 2^22 polls).  With a limit of a few polls the first wait of a
  * block usually runs out while its copies are still in flight: the block
  * stops issuing copies, skips its remaining outputs, waits (with the full
  * limit) for the copies it already issued, frees its tensor memory and sets

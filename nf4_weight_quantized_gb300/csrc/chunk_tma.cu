@@ -10,11 +10,15 @@
 //  * work units are (128-row tile, 256-column slice) pairs, tile-major; each of
 //    min(units, 152) persistent blocks takes one contiguous, equal share of them
 //    (stream-K), so every SM streams the same number of bytes;
-//  * one producer thread loads each unit with 2-D TMA copies: the codes (128 rows
-//    x 128 bytes, 128-byte swizzled so the dequantizing threads read them without
-//    bank conflicts), the 128 x 4 fp32 scales, and the four 64-column slices of X
-//    (32 rows, rows >= N zero-filled by the copy, already in the swizzled K-major
-//    layout the tensor core reads), into a ring of four stages;
+//  * two producer warps load each unit with 2-D TMA copies into two rings: one
+//    the codes (128 rows x 128 bytes, 128-byte swizzled so the dequantizing
+//    threads read them without bank conflicts) and the 128 x 4 fp32 scales into
+//    a ring of code stages that the dequantizing warps release as soon as they
+//    hold their bytes in registers; the other the four 64-column slices of
+//    X (32 rows, rows >= N zero-filled by the copy, already in the swizzled
+//    K-major layout the tensor core reads) into a ring of X stages that the
+//    MMA commit releases.  Code stages thus never wait for the tensor core, and
+//    the code ring runs several units ahead of the dequantization;
 //  * sixteen dequantizing warps turn each 64-column k-tile of codes into the bf16
 //    A operand (fp32 level x fp32 scale from the lane-replicated pair table,
 //    rounded once) and store it straight into tensor memory (tcgen05.st; row m
@@ -50,9 +54,13 @@ constexpr int EPI_WARPS = 4;   // warps 0-3: epilogue (TMEM lanes 32w .. 32w + 3
 constexpr int PROD_WARP = 4;
 constexpr int MMA_WARP = 5;
 constexpr int DQ_WARP0 = 6;
-constexpr int NTHREADS = (DQ_WARP0 + NDQ) * 32;  // 704
-#ifndef NF4_CHUNK_SR
-#define NF4_CHUNK_SR 4
+constexpr int XPROD_WARP = DQ_WARP0 + NDQ;       // 22: the X-ring producer
+constexpr int NTHREADS = (XPROD_WARP + 1) * 32;  // 736
+#ifndef NF4_CHUNK_SC
+#define NF4_CHUNK_SC 5
+#endif
+#ifndef NF4_CHUNK_SX
+#define NF4_CHUNK_SX 4
 #endif
 #ifndef NF4_CHUNK_SA
 #define NF4_CHUNK_SA 3
@@ -60,7 +68,8 @@ constexpr int NTHREADS = (DQ_WARP0 + NDQ) * 32;  // 704
 #ifndef NF4_DQ_SLEEP
 #define NF4_DQ_SLEEP 64
 #endif
-constexpr int SR = NF4_CHUNK_SR;  // raw stages (units) in shared memory
+constexpr int SC = NF4_CHUNK_SC;  // code stages (codes + scales of a unit) in shared memory
+constexpr int SX = NF4_CHUNK_SX;  // X stages (the unit's four X slices) in shared memory
 constexpr int SA = NF4_CHUNK_SA;  // A stages in tensor memory, KS k-tiles each
 // k-tiles per A stage: one barrier wait, KS x 4 MMAs and one commit per stage.
 // Measured alone, a wait + fence costs about 190 cycles and a commit 44
@@ -74,8 +83,9 @@ static_assert(KQ % KS == 0, "A stages tile a unit");
 constexpr int CODES_BYTES = TM * KQ * KT / 2;    // 16 KB
 constexpr int XT_BYTES = TN * KT * 2;            // 4 KB per k-tile
 constexpr int SCL_BYTES = TM * KQ * 4;           // 2 KB
-constexpr int RAW_BYTES = CODES_BYTES + KQ * XT_BYTES + SCL_BYTES;  // 34 KB
-constexpr int SMEM_BYTES = LUT_BYTES + SR * RAW_BYTES;
+constexpr int CST_BYTES = CODES_BYTES + SCL_BYTES;  // 18 KB code stage
+constexpr int XST_BYTES = KQ * XT_BYTES;            // 16 KB X stage
+constexpr int SMEM_BYTES = LUT_BYTES + SC * CST_BYTES + SX * XST_BYTES;
 static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory per block");
 // TMEM columns: two 32-column fp32 accumulators, then SA A stages of KS x 32
 // columns (64 bf16 of each row per k-tile, two per 32-bit column)
@@ -85,7 +95,7 @@ constexpr int TMEM_COLS = (A_COL0 + SA * A_COLS) <= 256 ? 256 : 512;  // a power
 static_assert(A_COL0 + SA * A_COLS <= TMEM_COLS, "tensor memory per block");
 constexpr int PLAN_SMS = 152;  // blocks planned for a 152-SM GB300 (the workspace depends on the shape only)
 
-static_assert(RAW_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+static_assert(CST_BYTES % 1024 == 0 && XST_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
 static_assert(NDQ == 16, "four dequantizing warps per 32-lane quarter of the tile, 16 columns each");
 
 struct StreamKArgs {
@@ -97,7 +107,7 @@ struct StreamKArgs {
   long long U;            // units = tiles * NQ
   int B;                  // blocks
   int maxseg;             // partial slots per tile (0: whole tiles per block)
-  uint32_t wait_polls;    // limit of the dequantizing warps' waits for staged units
+  uint32_t wait_polls;    // limit of the consumers' waits for staged codes and dequantized operands
 };
 
 // First unit of block b: an equal share of the units, or, when there are at
@@ -194,7 +204,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ unsigned int s_last;
-  __shared__ unsigned long long s_bar[2 * SR + 2 * SA + 4 + 1];
+  __shared__ unsigned long long s_bar[2 * SC + 2 * SX + 2 * SA + 4 + 1];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -203,20 +213,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const long long u1 = unit_start(blockIdx.x + 1, a);
   const int nq = (int)(u1 - u0);
 
-  uint8_t* raw0 = smem + LUT_BYTES;
+  uint8_t* cst0 = smem + LUT_BYTES;         // SC code stages: codes, then scales
+  uint8_t* xst0 = cst0 + SC * CST_BYTES;     // SX X stages
   const uint32_t bar0 = smem_addr(&s_bar[0]);
-  auto raw_full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-  auto raw_empty = [&](int s) { return bar0 + 8u * (uint32_t)(SR + s); };
-  auto a_full = [&](int s) { return bar0 + 8u * (uint32_t)(2 * SR + s); };
-  auto a_empty = [&](int s) { return bar0 + 8u * (uint32_t)(2 * SR + SA + s); };
-  auto acc_full = [&](int b) { return bar0 + 8u * (uint32_t)(2 * SR + 2 * SA + b); };
-  auto acc_empty = [&](int b) { return bar0 + 8u * (uint32_t)(2 * SR + 2 * SA + 2 + b); };
-  const uint32_t mma_done = bar0 + 8u * (uint32_t)(2 * SR + 2 * SA + 4);
+  constexpr int B_CE = SC, B_XF = 2 * SC, B_XE = 2 * SC + SX, B_AF = 2 * SC + 2 * SX, B_AE = B_AF + SA,
+                B_ACC = B_AE + SA;
+  auto c_full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto c_empty = [&](int s) { return bar0 + 8u * (uint32_t)(B_CE + s); };
+  auto x_full = [&](int s) { return bar0 + 8u * (uint32_t)(B_XF + s); };
+  auto x_empty = [&](int s) { return bar0 + 8u * (uint32_t)(B_XE + s); };
+  auto a_full = [&](int s) { return bar0 + 8u * (uint32_t)(B_AF + s); };
+  auto a_empty = [&](int s) { return bar0 + 8u * (uint32_t)(B_AE + s); };
+  auto acc_full = [&](int b) { return bar0 + 8u * (uint32_t)(B_ACC + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (uint32_t)(B_ACC + 2 + b); };
+  const uint32_t mma_done = bar0 + 8u * (uint32_t)(B_ACC + 4);
 
   if (tid == 0) {
-    for (int s = 0; s < SR; ++s) {
-      mbar_init(raw_full(s), 1);
-      mbar_init(raw_empty(s), NDQ + 1);  // the dequantizing warps and the MMA commit
+    for (int s = 0; s < SC; ++s) {
+      mbar_init(c_full(s), 1);
+      mbar_init(c_empty(s), NDQ);  // the dequantizing warps, once their codes are in registers
+    }
+    for (int s = 0; s < SX; ++s) {
+      mbar_init(x_full(s), 1);
+      mbar_init(x_empty(s), 1);  // the MMA commit of the unit
     }
     for (int s = 0; s < SA; ++s) {
       mbar_init(a_full(s), NDQ);
@@ -245,54 +264,75 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem = s_tmem;
 
-  // producer: one unit = the codes, the four X slices and the scales of a
-  // 128-row x 256-column slice, all completing on the stage's full barrier
-  auto issue_unit = [&](int q) {
-    const int s = q % SR;
+  // producers: a unit is the codes and scales of a 128-row x 256-column slice
+  // (code ring) and the four 64-column slices of X it multiplies (X ring),
+  // each completing on its stage's full barrier
+  auto issue_codes = [&](int q) {
+    const int s = q % SC;
     const long long u = u0 + q;
     const int tile = (int)(u / a.NQ), kq = (int)(u % a.NQ);
-    uint8_t* raw = raw0 + s * RAW_BYTES;
-    mbar_arrive_expect_tx(raw_full(s), RAW_BYTES);
-    tma_load_2d(smem_addr(raw), &tm_codes, kq * 128, tile * TM, raw_full(s));
+    uint8_t* st = cst0 + s * CST_BYTES;
+    mbar_arrive_expect_tx(c_full(s), CST_BYTES);
+    tma_load_2d(smem_addr(st), &tm_codes, kq * 128, tile * TM, c_full(s));
+    tma_load_2d(smem_addr(st + CODES_BYTES), &tm_scales, kq * KQ, tile * TM, c_full(s));
+  };
+  auto issue_x = [&](int q) {
+    const int s = q % SX;
+    const int kq = (int)((u0 + q) % a.NQ);
+    uint8_t* st = xst0 + s * XST_BYTES;
+    mbar_arrive_expect_tx(x_full(s), XST_BYTES);
 #pragma unroll
-    for (int i = 0; i < KQ; ++i)
-      tma_load_2d(smem_addr(raw + CODES_BYTES + i * XT_BYTES), &tm_x, (kq * KQ + i) * KT, 0, raw_full(s));
-    tma_load_2d(smem_addr(raw + CODES_BYTES + KQ * XT_BYTES), &tm_scales, kq * KQ, tile * TM, raw_full(s));
+    for (int i = 0; i < KQ; ++i) tma_load_2d(smem_addr(st + i * XT_BYTES), &tm_x, (kq * KQ + i) * KT, 0, x_full(s));
   };
   // the first stages go out before the pair table is built, so the table
   // build hides under their latency
-  const int pre = (smem_addr(raw0) & 1023u) == 0 ? (nq < SR ? nq : SR) : 0;
+  const bool aligned1k = (smem_addr(cst0) & 1023u) == 0;
+  const int pre_c = aligned1k ? (nq < SC ? nq : SC) : 0;
+  const int pre_x = aligned1k ? (nq < SX ? nq : SX) : 0;
   if (warp == PROD_WARP && lane == 0)
-    for (int q = 0; q < pre; ++q) issue_unit(q);
+    for (int q = 0; q < pre_c; ++q) issue_codes(q);
+  if (warp == XPROD_WARP && lane == 0)
+    for (int q = 0; q < pre_x; ++q) issue_x(q);
   // pair table: byte b, lane l -> (cb[b & 15], cb[b >> 4]) at b * 256 + l * 8
   for (int i = tid; i < LUT_BYTES / 8; i += NTHREADS) {
     const int b = i >> 5;
     reinterpret_cast<float2*>(smem)[i] = make_float2(cbs[b & 15], cbs[b >> 4]);
   }
-  if (tid == 0 && (smem_addr(raw0) & 1023u) != 0) {  // swizzled tiles need 1024-byte alignment
+  if (tid == 0 && !aligned1k) {  // swizzled tiles need 1024-byte alignment
     s_abort = 1;
     atomicOr(&g_nf4_device_error, kErrWaitTimeout);
   }
   __syncthreads();
   volatile int* abort = &s_abort;
 
-  if (warp == PROD_WARP) {
-    // ------------------------------------------------------------ producer
-    // The whole warp runs the loop; lane 0 issues.
-    int issued = pre;
-    for (int q = pre; q < nq; ++q) {
-      const int s = q % SR;
-      if (q >= SR && !mbar_wait_warp(raw_empty(s), (uint32_t)(((q / SR) - 1) & 1), abort, lane, 64)) break;
-      if (__any_sync(0xffffffffu, *abort != 0)) break;  // warp-uniform
-      if (lane == 0) issue_unit(q);
-      __syncwarp();
-      issued = q + 1;
-    }
-    if (*abort && lane == 0) {
-      // wait (bounded, ignoring the flag) for the copies still in flight
-      for (int q = (issued > SR ? issued - SR : 0); q < issued; ++q)
-        for (uint32_t i = 0; i < kWaitPolls; ++i)
-          if (mbar_try_wait(raw_full(q % SR), (uint32_t)((q / SR) & 1))) break;
+  if (warp == PROD_WARP || warp == XPROD_WARP) {
+    // ------------------------------------------------------------ producers
+    // lane 0 of one warp fills the code ring, lane 0 of the other the X ring,
+    // each waiting only for its own ring's stages to be released
+    if (lane == 0) {
+      const bool codes_lane = warp == PROD_WARP;
+      const int ring = codes_lane ? SC : SX;
+      int issued = codes_lane ? pre_c : pre_x;
+      for (int q = issued; q < nq; ++q) {
+        const int s = q % ring;
+        if (q >= ring &&
+            !mbar_wait_sleep(codes_lane ? c_empty(s) : x_empty(s), (uint32_t)(((q / ring) - 1) & 1), abort, 64))
+          break;
+        if (*abort) break;
+        if (codes_lane)
+          issue_codes(q);
+        else
+          issue_x(q);
+        issued = q + 1;
+      }
+      if (*abort) {
+        // wait (bounded, ignoring the flag) for this lane's copies still in flight
+        for (int q = (issued > ring ? issued - ring : 0); q < issued; ++q) {
+          const uint32_t fb = codes_lane ? c_full(q % ring) : x_full(q % ring);
+          for (uint32_t i = 0; i < kWaitPolls; ++i)
+            if (mbar_try_wait(fb, (uint32_t)((q / ring) & 1))) break;
+        }
+      }
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
@@ -310,12 +350,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after_sync();
         const uint32_t dtm = tmem + (uint32_t)(buf * TN);
         for (; q < qe; ++q) {
-          const int s = q % SR;
-          mbar_wait_warp(raw_full(s), (uint32_t)((q / SR) & 1), abort, lane, 0);
-          const uint32_t xb = smem_addr(raw0 + s * RAW_BYTES + CODES_BYTES);
+          const int s = q % SX;
+          mbar_wait_warp(x_full(s), (uint32_t)((q / SX) & 1), abort, lane, 0);
+          const uint32_t xb = smem_addr(xst0 + s * XST_BYTES);
           for (int h = 0; h < KQ / KS; ++h, ++j) {
             const int as = j % SA;
-            mbar_wait_warp(a_full(as), (uint32_t)((j / SA) & 1), abort, lane, 0);
+            mbar_wait_warp(a_full(as), (uint32_t)((j / SA) & 1), abort, lane, 0, a.wait_polls);
             tc_fence_after_sync();
             if (lane == 0) {
               if (!*abort) {
@@ -332,7 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             __syncwarp();
           }
-          if (lane == 0) tc_commit(raw_empty(s));  // X of this unit is read once these MMAs complete
+          if (lane == 0) tc_commit(x_empty(s));  // X of this unit is read once these MMAs complete
           __syncwarp();
         }
         if (lane == 0) tc_commit(acc_full(buf));
@@ -347,7 +387,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       __syncwarp();
     }
-  } else if (warp >= DQ_WARP0) {
+  } else if (warp >= DQ_WARP0 && warp < DQ_WARP0 + NDQ) {
     // ---------------------------------------------------- dequantization
     // A warp may reach only TMEM lanes 32 (warp % 4) .. + 31, so each thread owns
     // one tile row (its TMEM lane) and a 16-column group of every k-tile (the
@@ -358,11 +398,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t laneoff = (uint32_t)lane * 8u;  // pair-table replica
     int j = 0;
     for (int q = 0; q < nq; ++q) {
-      const int s = q % SR;
-      mbar_wait_warp(raw_full(s), (uint32_t)((q / SR) & 1), abort, lane, NF4_DQ_SLEEP, a.wait_polls);
-      const uint8_t* raw = raw0 + s * RAW_BYTES;
-      const float4 sc4 = *reinterpret_cast<const float4*>(raw + CODES_BYTES + KQ * XT_BYTES + r * 16);
+      const int s = q % SC;
+      mbar_wait_warp(c_full(s), (uint32_t)((q / SC) & 1), abort, lane, NF4_DQ_SLEEP, a.wait_polls);
+      const uint8_t* cst = cst0 + s * CST_BYTES;
+      // this thread's codes (8 bytes of each k-tile) and scales, into
+      // registers; then the code stage goes back to the producer at once
+      const float4 sc4 = *reinterpret_cast<const float4*>(cst + CODES_BYTES + r * 16);
       const float scl[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+      uint2 cw4[KQ];
+#pragma unroll
+      for (int i = 0; i < KQ; ++i) cw4[i] = lds64(cst + r * 128 + (((2 * i + (cg >> 1)) ^ (r & 7)) << 4) + (cg & 1) * 8);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c_empty(s));
 #pragma unroll
       for (int h = 0; h < KQ / KS; ++h, ++j) {
         const int as = j % SA;
@@ -373,8 +420,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i2 = 0; i2 < KS; ++i2) {
           const int i = h * KS + i2;
           uint32_t p[8];
-          const uint2 cw = lds64(raw + r * 128 + (((2 * i + (cg >> 1)) ^ (r & 7)) << 4) + (cg & 1) * 8);
-          const uint32_t w2[2] = {cw.x, cw.y};
+          const uint32_t w2[2] = {cw4[i].x, cw4[i].y};
 #pragma unroll
           for (int e = 0; e < 2; ++e)
 #pragma unroll
@@ -392,8 +438,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(a_full(as));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(raw_empty(s));
     }
   } else {
     // --------------------------------------------------------- epilogue
@@ -585,9 +629,9 @@ std::string describe_chunk_tma(int64_t M, int64_t K, int N) {
   std::snprintf(buf, sizeof buf,
                 "chunk M=%lld K=%lld N=%d: tcgen05 M=%d N=%d K=16, %s over %lld units of 128 rows x 256 "
                 "columns on %d persistent blocks (%d threads: %d dequantizing warps, TMA producer, MMA issuer, 4 "
-                "epilogue warps), %d raw + %d operand stages, 2 TMEM accumulators",
+                "epilogue warps), %d code + %d X + %d operand stages, 2 TMEM accumulators",
                 (long long)M, (long long)K, N, TM, TN, p.maxseg == 0 ? "whole tiles per block" : "stream-K", p.U, p.B,
-                NTHREADS, NDQ, SR, SA);
+                NTHREADS, NDQ, SC, SX, SA);
   return buf;
 }
 

@@ -181,9 +181,10 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
 // turns it off).
 bool pdl_enabled();
 
-// Host: poll limit of the kernels' waits for their weight data to arrive
-// (kWaitPolls unless nf4_debug_set_wait_limit set another).  Waits that drain
-// copies already in flight always keep kWaitPolls.
+// Host: poll limit of the consumers' waits for staged weights and dequantized
+// operands (kWaitPolls unless nf4_debug_set_wait_limit set another).  Waits
+// that drain copies or tensor-core work already in flight always keep
+// kWaitPolls.
 uint32_t data_wait_polls();
 
 __device__ __forceinline__ uint4 lds128(const void* p) {

@@ -1,11 +1,12 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out.
 
 Every wait of the bulk-copy GEMV and of the TMA prefill-chunk kernel on a
-shared-memory barrier is bounded.  nf4_debug_set_wait_limit shortens the waits
-for staged weights to one non-blocking poll, on an ordinary valid call whose
-copies all complete: the blocks whose data has not landed at that poll give
-up, skip their outputs, wait (with the full limit) for the copies they issued,
-free their tensor memory and set the error word.  The tests check that
+shared-memory barrier is bounded.  nf4_debug_set_wait_limit shortens the
+consumers' waits (for staged weights, and in the chunk for the dequantized
+operand the tensor core reads) to one non-blocking poll, on an ordinary valid
+call whose copies all complete: a block whose data is not there at that poll
+gives up, skips its outputs, waits (with the full limit) for the copies and
+tensor-core work it issued, frees its tensor memory and sets the error word.  The tests check that
 nf4_check_device_errors reports NF4_ETIMEOUT, that whatever the GEMV did write
 is still correct, and that the next ordinary call in the same process is
 correct and clean.  Nothing waits on a flag that is never set and nothing
