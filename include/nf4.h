@@ -284,13 +284,14 @@ nf4_status nf4_check_device_errors(void);
 /*
  * Diagnostic for failure-detection tests; never needed for correct results.
  * Sets how many times the bulk-copy GEMV and the TMA prefill-chunk kernels
- * poll for their staged weights (and, in the chunk, for the dequantized
- * operand the tensor core reads) before giving up (0 restores the default,
- * 2^22 polls).  With a limit of a few polls the first wait of a
- * block usually runs out while its copies are still in flight: the block
- * stops issuing copies, skips its remaining outputs, waits (with the full
- * limit) for the copies it already issued, frees its tensor memory and sets
- * the error word that nf4_check_device_errors() reports as NF4_ETIMEOUT.
+ * poll a pipeline barrier (a producer waiting for a free stage, a consumer
+ * for staged weights or, in the chunk, for the dequantized operand the
+ * tensor core reads) before giving up (0 restores the default, 2^22 polls).
+ * With a limit of a few polls a block's producer runs out as soon as its
+ * ring is full (its consumers are still computing): the block stops issuing
+ * copies, skips its remaining outputs, waits (with the full limit) for the
+ * copies and tensor-core work it already issued, frees its tensor memory and
+ * sets the error word that nf4_check_device_errors() reports as NF4_ETIMEOUT.
  * Outputs of such a call are invalid; workspaces are left zeroed as usual.
  * Process-wide; applies to calls launched afterwards.
  */

@@ -25,8 +25,10 @@
 //    in TMEM lane m), a ring of three stages of four k-tiles: the A operand never passes
 //    through shared memory, which the pair-table reads alone keep busy;
 //  * one thread issues tcgen05.mma (M = 128, N = 32, K = 16, A from TMEM, X from
-//    shared memory) into one of two 32-column TMEM accumulators, so four
-//    epilogue warps can drain one tile while the next accumulates;
+//    shared memory) into one of two TMEM accumulator buffers, so four epilogue
+//    warps can drain one tile while the next accumulates; each buffer holds
+//    two 32-column chains that consecutive MMAs alternate between (an MMA
+//    never waits for the previous one's accumulation), added in the epilogue;
 //  * a tile whose K range is split over several blocks is finished by the last of
 //    them to arrive (a per-tile ticket), which adds the partial tiles in block
 //    order: the result does not depend on timing.
@@ -55,7 +57,8 @@ constexpr int PROD_WARP = 4;
 constexpr int MMA_WARP = 5;
 constexpr int DQ_WARP0 = 6;
 constexpr int XPROD_WARP = DQ_WARP0 + NDQ;       // 22: the X-ring producer
-constexpr int NTHREADS = (XPROD_WARP + 1) * 32;  // 736
+constexpr int MMA2_WARP = XPROD_WARP + 1;        // 23: the second MMA issuer
+constexpr int NTHREADS = (MMA2_WARP + 1) * 32;   // 768
 #ifndef NF4_CHUNK_SC
 #define NF4_CHUNK_SC 5
 #endif
@@ -90,7 +93,11 @@ static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory per block");
 // TMEM columns: two 32-column fp32 accumulators, then SA A stages of KS x 32
 // columns (64 bf16 of each row per k-tile, two per 32-bit column)
 constexpr int A_COLS = KS * KT / 2;
-constexpr int A_COL0 = 2 * TN;
+// Accumulators: two buffers (one tile accumulates while the epilogue drains
+// the other) of CH = 2 chains, one per MMA issuer warp: columns
+// (buf * CH + issuer) * TN.
+constexpr int CH = 2;
+constexpr int A_COL0 = 2 * CH * TN;
 constexpr int TMEM_COLS = (A_COL0 + SA * A_COLS) <= 256 ? 256 : 512;  // a power of two; one block per SM
 static_assert(A_COL0 + SA * A_COLS <= TMEM_COLS, "tensor memory per block");
 constexpr int PLAN_SMS = 152;  // blocks planned for a 152-SM GB300 (the workspace depends on the shape only)
@@ -107,7 +114,7 @@ struct StreamKArgs {
   long long U;            // units = tiles * NQ
   int B;                  // blocks
   int maxseg;             // partial slots per tile (0: whole tiles per block)
-  uint32_t wait_polls;    // limit of the consumers' waits for staged codes and dequantized operands
+  uint32_t wait_polls;    // limit of the pipeline waits (free stages, staged codes, dequantized operands)
 };
 
 // First unit of block b: an equal share of the units, or, when there are at
@@ -141,13 +148,18 @@ __device__ __forceinline__ uint2 lds64(const void* p) {
 
 // D[tmem] (+)= A[tmem] * B[smem desc]^T, bf16 inputs, fp32 accumulate; A is
 // M rows in TMEM lanes, each row's K values packed two per 32-bit column.
-__device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
+// The B descriptor comes as its two 32-bit halves: the issuer precomputes the
+// high half (layout constants) and the low half of a stage's first k-step,
+// so each MMA of a stage costs one 32-bit add (the start-address field, bits
+// 0-13, never carries: shared addresses are below 256 KB).
+__device__ __forceinline__ void tc_mma_bf16_ta2(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -191,6 +203,17 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
+}
+
+// Warp-wide load of 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -242,10 +265,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(a_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(acc_full(b), 1);
+      mbar_init(acc_full(b), 2);  // one commit per MMA issuer
       mbar_init(acc_empty(b), EPI_WARPS);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, 2);
     mbar_init_fence();
     s_abort = 0;
   }
@@ -316,7 +339,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int q = issued; q < nq; ++q) {
         const int s = q % ring;
         if (q >= ring &&
-            !mbar_wait_sleep(codes_lane ? c_empty(s) : x_empty(s), (uint32_t)(((q / ring) - 1) & 1), abort, 64))
+            !mbar_wait_sleep(codes_lane ? c_empty(s) : x_empty(s), (uint32_t)(((q / ring) - 1) & 1), abort, 64,
+                             a.wait_polls))
           break;
         if (*abort) break;
         if (codes_lane)
@@ -335,12 +359,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // -------------------------------------------------------- MMA issuer
-    // the whole warp runs the loop, lane 0 issues the tensor-core operations
+  } else if (warp == MMA_WARP || warp == MMA2_WARP) {
+    // ------------------------------------------------------- MMA issuers
+    // Two issuer warps: within a tile, units alternate between them (unit
+    // qs + 2i + me goes to issuer me), each into its own accumulator chain, so
+    // while one warp waits out an MMA issue the other issues.  The whole warp
+    // runs the loop; lane 0 issues the tensor-core operations.
     {
+      const int me = warp == MMA_WARP ? 0 : 1;
       const uint32_t idesc = idesc_bf16_f32(TM, TN);
-      int j = 0, g = 0;
+      int g = 0;
       for (int q = 0; q < nq;) {
         const long long tile = (u0 + q) / a.NQ;
         const int qs = q;
@@ -348,40 +376,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int buf = g & 1;
         if (g >= 2) mbar_wait_warp(acc_empty(buf), (uint32_t)(((g >> 1) - 1) & 1), abort, lane, 0);
         tc_fence_after_sync();
-        const uint32_t dtm = tmem + (uint32_t)(buf * TN);
-        for (; q < qe; ++q) {
+        const uint32_t dtm = tmem + (uint32_t)((buf * CH + me) * TN);
+        bool first = true;  // this issuer's first k-step of the tile starts its chain at 0
+        for (q = qs + me; q < qe; q += CH) {
           const int s = q % SX;
           mbar_wait_warp(x_full(s), (uint32_t)((q / SX) & 1), abort, lane, 0);
           const uint32_t xb = smem_addr(xst0 + s * XST_BYTES);
-          for (int h = 0; h < KQ / KS; ++h, ++j) {
+#pragma unroll 1
+          for (int h = 0; h < KQ / KS; ++h) {
+            const int j = q * (KQ / KS) + h;  // A stages are filled in unit order
             const int as = j % SA;
             mbar_wait_warp(a_full(as), (uint32_t)((j / SA) & 1), abort, lane, 0, a.wait_polls);
             tc_fence_after_sync();
             if (lane == 0) {
               if (!*abort) {
                 const uint32_t at = tmem + (uint32_t)(A_COL0 + as * A_COLS);
+                const uint64_t d0 = smem_desc_sw128(xb + h * KS * XT_BYTES);
+                const uint32_t blo = (uint32_t)d0, bhi = (uint32_t)(d0 >> 32);
 #pragma unroll
                 for (int i2 = 0; i2 < KS; ++i2)
 #pragma unroll
                   for (int kk = 0; kk < KT / 16; ++kk)
-                    tc_mma_bf16_ta(dtm, at + i2 * (KT / 2) + kk * 8,
-                                   smem_desc_sw128(xb + (h * KS + i2) * XT_BYTES + kk * 32), idesc,
-                                   (q > qs || h > 0 || i2 > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_bf16_ta2(dtm, at + i2 * (KT / 2) + kk * 8, blo + (uint32_t)((i2 * XT_BYTES + kk * 32) >> 4),
+                                    bhi, idesc, (!first || i2 > 0 || kk > 0) ? 1u : 0u);
               }
               tc_commit(a_empty(as));
             }
+            first = false;
             __syncwarp();
           }
           if (lane == 0) tc_commit(x_empty(s));  // X of this unit is read once these MMAs complete
           __syncwarp();
         }
-        if (lane == 0) tc_commit(acc_full(buf));
+        q = qe;
+        if (lane == 0) tc_commit(acc_full(buf));  // both issuers arrive once per tile
         __syncwarp();
         ++g;
       }
       // every tensor-core operation has completed before TMEM is freed
       if (lane == 0) {
-        tc_commit(mma_done);
+        tc_commit(mma_done);  // both issuers arrive
         for (uint32_t i = 0; i < kWaitPolls; ++i)
           if (mbar_try_wait(mma_done, 0)) break;
       }
@@ -446,12 +480,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int q = 0; q < nq; ++g) {
       const long long tile = (u0 + q) / a.NQ;
       const int qe = (int)((tile + 1) * a.NQ - u0 < nq ? (tile + 1) * a.NQ - u0 : nq);
+      const bool two = qe - q >= 2;  // the second issuer's chain holds units of this tile
       q = qe;
       const int buf = g & 1;
       const bool ok = mbar_wait_warp(acc_full(buf), (uint32_t)((g >> 1) & 1), abort, lane, 128);
       tc_fence_after_sync();
       uint32_t acc[32];
-      tmem_ld_32x32b_x32(tmem + (uint32_t)(buf * TN) + ((uint32_t)(warp * 32) << 16), acc);
+      tmem_ld_32x32b_x32(tmem + (uint32_t)(buf * CH * TN) + ((uint32_t)(warp * 32) << 16), acc);
+      if (two) {  // the two issuers' chains, added once (the second in halves)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t acc1[16];
+          tmem_ld_32x32b_x16(tmem + (uint32_t)((buf * CH + 1) * TN + 16 * half) + ((uint32_t)(warp * 32) << 16), acc1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int n = 0; n < 16; ++n)
+            acc[16 * half + n] = __float_as_uint(__uint_as_float(acc[16 * half + n]) + __uint_as_float(acc1[n]));
+        }
+      }
       tmem_ld_wait();
       tc_fence_before_sync();
       __syncwarp();

@@ -181,10 +181,11 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
 // turns it off).
 bool pdl_enabled();
 
-// Host: poll limit of the consumers' waits for staged weights and dequantized
-// operands (kWaitPolls unless nf4_debug_set_wait_limit set another).  Waits
-// that drain copies or tensor-core work already in flight always keep
-// kWaitPolls.
+// Host: poll limit of the pipeline waits between producers and consumers (a
+// producer's wait for a free stage, a consumer's wait for staged weights or
+// dequantized operands): kWaitPolls unless nf4_debug_set_wait_limit set
+// another.  Waits that drain copies or tensor-core work already in flight
+// always keep kWaitPolls.
 uint32_t data_wait_polls();
 
 __device__ __forceinline__ uint4 lds128(const void* p) {
@@ -371,7 +372,7 @@ struct GemvArgs {
   int K;
   int G;    // threads cooperating on one row (multiple of 32)
   int gpc;  // row groups per block
-  uint32_t wait_polls;  // limit of the waits for staged weights (data_wait_polls)
+  uint32_t wait_polls;  // limit of the pipeline waits between producer and consumers (data_wait_polls)
   Codebook cb;
   // fused q/k/v (EPI_QKV): one row space over three matrices sharing x; rows
   // [0, seg_end[0]) are matrix 0's, [seg_end[0], seg_end[1]) matrix 1's,

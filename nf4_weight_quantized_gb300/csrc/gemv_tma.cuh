@@ -324,7 +324,7 @@ __global__ void gemv_tma_kernel(const __grid_constant__ GemvArgs a, const __grid
       for (; issued < n_it; ++issued) {
         const int s = issued % P.S;
         // the consumers released this stage's previous use (iteration issued - S)
-        if (!mbar_wait_bounded(empty_bar(s), (uint32_t)(((issued / P.S) - 1) & 1), abort)) break;
+        if (!mbar_wait_bounded(empty_bar(s), (uint32_t)(((issued / P.S) - 1) & 1), abort, a.wait_polls)) break;
         issue(issued);
       }
       if (*abort) {

@@ -2,10 +2,12 @@
 
 Every wait of the bulk-copy GEMV and of the TMA prefill-chunk kernel on a
 shared-memory barrier is bounded.  nf4_debug_set_wait_limit shortens the
-consumers' waits (for staged weights, and in the chunk for the dequantized
-operand the tensor core reads) to one non-blocking poll, on an ordinary valid
-call whose copies all complete: a block whose data is not there at that poll
-gives up, skips its outputs, waits (with the full limit) for the copies and
+pipeline waits (a producer's wait for a free stage, a consumer's wait for
+staged weights or dequantized operands) to one non-blocking poll, on an
+ordinary valid call whose copies all complete.  A producer that has filled its
+ring always finds the next stage still in use at that poll (its consumers are
+computing), so every block whose rows need more stages than its ring holds
+gives up: it skips its outputs, waits (with the full limit) for the copies and
 tensor-core work it issued, frees its tensor memory and sets the error word.  The tests check that
 nf4_check_device_errors reports NF4_ETIMEOUT, that whatever the GEMV did write
 is still correct, and that the next ordinary call in the same process is
