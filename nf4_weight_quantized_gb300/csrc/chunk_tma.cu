@@ -170,8 +170,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
-// (r0, r1) = (a0 * b, a1 * b), each product rounded to nearest even: one
-// packed fp32 multiply instead of two.
 __device__ __forceinline__ void mul2_f32(float& r0, float& r1, float a0, float a1, float b) {
   asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\t"
       "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
@@ -273,6 +271,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     s_abort = 0;
   }
   if (tid < 16) cbs[tid] = cbk.v[tid];
+  pdl_launch_dependents();  // the next kernel may start its prologue on SMs this grid has left
   if (warp == MMA_WARP) {
     tmem_alloc(smem_addr(&s_tmem), TMEM_COLS);
     tmem_relinquish();
@@ -307,15 +306,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
     for (int i = 0; i < KQ; ++i) tma_load_2d(smem_addr(st + i * XT_BYTES), &tm_x, (kq * KQ + i) * KT, 0, x_full(s));
   };
-  // the first stages go out before the pair table is built, so the table
-  // build hides under their latency
+  // the first code stages go out before the pair table is built, so the
+  // table build hides under their latency
   const bool aligned1k = (smem_addr(cst0) & 1023u) == 0;
   const int pre_c = aligned1k ? (nq < SC ? nq : SC) : 0;
-  const int pre_x = aligned1k ? (nq < SX ? nq : SX) : 0;
   if (warp == PROD_WARP && lane == 0)
     for (int q = 0; q < pre_c; ++q) issue_codes(q);
-  if (warp == XPROD_WARP && lane == 0)
-    for (int q = 0; q < pre_x; ++q) issue_x(q);
+  // (X is the previous kernel's output: its first slices go out after the
+  // dependency wait, in the X producer's loop below)
   // pair table: byte b, lane l -> (cb[b & 15], cb[b >> 4]) at b * 256 + l * 8
   for (int i = tid; i < LUT_BYTES / 8; i += NTHREADS) {
     const int b = i >> 5;
@@ -335,7 +333,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       const bool codes_lane = warp == PROD_WARP;
       const int ring = codes_lane ? SC : SX;
-      int issued = codes_lane ? pre_c : pre_x;
+      // programmatic dependent launch: the weights never depend on the
+      // previous kernel, X does
+      if (!codes_lane) pdl_wait();
+      int issued = codes_lane ? pre_c : 0;
       for (int q = issued; q < nq; ++q) {
         const int s = q % ring;
         if (q >= ring &&
@@ -476,6 +477,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     // --------------------------------------------------------- epilogue
     const int er = warp * 32 + lane;  // tile row = TMEM lane
+    pdl_wait();  // Y and the workspace are written only after the previous kernel has finished
     int g = 0;
     for (int q = 0; q < nq; ++g) {
       const long long tile = (u0 + q) / a.NQ;
@@ -665,19 +667,31 @@ cudaError_t launch_chunk_tma(const uint8_t* codes, const float* scales, int M, i
   a.maxseg = p.maxseg;
   a.wait_polls = data_wait_polls();
   return checked_launch(reinterpret_cast<const void*>(&chunk_tma_kernel), NTHREADS, SMEM_BYTES, [&] {
-    chunk_tma_kernel<<<p.B, NTHREADS, SMEM_BYTES, s>>>(mc, ms, mx, a, cb);
+    // programmatic dependent launch: blocks may start (TMEM, barriers, pair
+    // table, the first code stages) while the previous kernel finishes
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)p.B);
+    cfg.blockDim = dim3((unsigned)NTHREADS);
+    cfg.dynamicSmemBytes = (size_t)SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cudaLaunchKernelEx(&cfg, chunk_tma_kernel, mc, ms, mx, a, cb);
   });
 }
 
 std::string describe_chunk_tma(int64_t M, int64_t K, int N) {
   const Plan p = plan_for(M, K);
-  char buf[320];
+  char buf[448];
   std::snprintf(buf, sizeof buf,
                 "chunk M=%lld K=%lld N=%d: tcgen05 M=%d N=%d K=16, %s over %lld units of 128 rows x 256 "
-                "columns on %d persistent blocks (%d threads: %d dequantizing warps, TMA producer, MMA issuer, 4 "
-                "epilogue warps), %d code + %d X + %d operand stages, 2 TMEM accumulators",
+                "columns on %d persistent blocks (%d threads: %d dequantizing warps, 2 TMA producers, 2 MMA issuers, 4 "
+                "epilogue warps), %d code + %d X + %d operand stages, 2 TMEM accumulator buffers of 2 chains, %s",
                 (long long)M, (long long)K, N, TM, TN, p.maxseg == 0 ? "whole tiles per block" : "stream-K", p.U, p.B,
-                NTHREADS, NDQ, SC, SX, SA);
+                NTHREADS, NDQ, SC, SX, SA, pdl_enabled() ? "programmatic dependent launch" : "plain launch");
   return buf;
 }
 
