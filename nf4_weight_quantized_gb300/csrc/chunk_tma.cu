@@ -536,14 +536,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // loads per slot, not one round trip per value); slots added in order
         const float* base = a.partial + (long long)tile * a.maxseg * a.N * TM;
         float sum[TN];
-#pragma unroll
-        for (int n = 0; n < TN; ++n) sum[n] = 0.f;
-        for (int k = 0; k < nseg; ++k) {
+        if (nseg == 2) {
+          // the usual split: this block's own partial is still in registers,
+          // so one slot is loaded; added in block order from 0 as below
           float v[TN];
 #pragma unroll
-          for (int n = 0; n < TN; ++n) v[n] = n < a.N ? __ldcg(base + ((long long)k * a.N + n) * TM + er) : 0.f;
+          for (int n = 0; n < TN; ++n) v[n] = n < a.N ? __ldcg(base + ((long long)(1 - si) * a.N + n) * TM + er) : 0.f;
 #pragma unroll
-          for (int n = 0; n < TN; ++n) sum[n] += v[n];
+          for (int n = 0; n < TN; ++n)
+            sum[n] = si == 0 ? (0.f + __uint_as_float(acc[n])) + v[n] : (0.f + v[n]) + __uint_as_float(acc[n]);
+        } else {
+#pragma unroll
+          for (int n = 0; n < TN; ++n) sum[n] = 0.f;
+          for (int k = 0; k < nseg; ++k) {
+            float v[TN];
+#pragma unroll
+            for (int n = 0; n < TN; ++n) v[n] = n < a.N ? __ldcg(base + ((long long)k * a.N + n) * TM + er) : 0.f;
+#pragma unroll
+            for (int n = 0; n < TN; ++n) sum[n] += v[n];
+          }
         }
         if (!*abort && m < a.M) {
 #pragma unroll
