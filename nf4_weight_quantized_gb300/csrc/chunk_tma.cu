@@ -214,6 +214,10 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+// Release and acquire at GPU scope (orders this thread's, and by cumulativity
+// the CTA-barrier-ordered, memory operations around a ticket atomic).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -523,15 +527,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int n = 0; n < TN; ++n)
           if (n < a.N) slot[n * TM + er] = __uint_as_float(acc[n]);
       }
-      __threadfence();
+      // Publish the partial: the barrier orders every epilogue thread's stores
+      // before thread 0, whose release fence (cumulative) then precedes its
+      // ticket; the last arriver's acquire fence follows its ticket, and the
+      // barrier orders it before every thread's loads of the other partials.
       named_bar_sync(1, EPI_WARPS * 32);
       if (tid == 0) {
+        fence_acq_rel_gpu();
         const unsigned int prev = atomicAdd(&a.tickets[tile], 1u);
         s_last = (prev == (unsigned int)nseg - 1) ? 1u : 0u;
+        if (s_last) fence_acq_rel_gpu();
       }
       named_bar_sync(1, EPI_WARPS * 32);
       if (s_last) {
-        __threadfence();
         // all of a slot's values are loaded before any store (32 independent
         // loads per slot, not one round trip per value); slots added in order
         const float* base = a.partial + (long long)tile * a.maxseg * a.N * TM;
