@@ -211,8 +211,14 @@ TmaConfig choose_tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int devi
     c.nch = 1;
     c.G = 32;
   } else if (H <= 64) {
-    // one warp per row, two chunks per thread: no cross-warp reduction
-    c.nch = env_int("NF4_TMA_NCH", 2);
+    // one warp per row, two chunks per thread (no cross-warp reduction), or
+    // for many rows of one matrix two warps per row, one chunk per thread
+    // (more warps to hide the pair-table loads; measured with fp32 levels:
+    // 151936 x 2048 48.5 against 49.7 us, 22016 x 2048 interleaved gate/up
+    // 11.0 against 12.2 us; the two-matrix SwiGLU keeps two chunks, 10.6
+    // against 12.0 us)
+    const bool many_rows = M >= 16384 && epi != EPI_SWIGLU;
+    c.nch = env_int("NF4_TMA_NCH", many_rows ? 1 : 2);
     c.G = c.nch == 2 ? 32 : 64;
   } else if (32 * ((H + 31) / 32) <= 992 && env_int("NF4_TMA_NCH", 1) == 1) {
     c.nch = 1;
@@ -229,14 +235,11 @@ TmaConfig choose_tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int devi
   // pair table
   c.rb = c.nch == 1 ? 8 : 4;
   while (c.rb > 2 && 2 * c.rb * nv * (int)(K / 2 + K / 16) > 150 * 1024) c.rb /= 2;
-  // two chunks per thread and few rows per block (short kernels): 2 rows per
-  // stage start the computation sooner (measured: 2048 x 2048 and SwiGLU
-  // 11008 x 2048 are faster, lm_head's 151936 rows are not)
-  {
-    int sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    if (c.nch == 2 && M < 512LL * (sms > 0 ? sms : 1)) c.rb = 2;
-  }
+  // two chunks per thread and few rows (short kernels): 2 rows per stage start
+  // the computation sooner (measured with fp32 levels: 2048 x 2048 3.48
+  // against 3.44 us, the fused 3B q/k/v 3.95 against 4.14, 256 x 2048 2.68
+  // against 3.33; SwiGLU's 11008 rows are faster with 4: 10.6 against 11.2)
+  if (c.nch == 2 && M < 4096) c.rb = 2;
   c.rb = env_int("NF4_TMA_RB", c.rb);
   // every activation dtype uses the exact fp32 levels; NF4_LUT=1 opts bf16
   // activations into the narrower fp16-level mixed-precision loop
