@@ -227,8 +227,6 @@ TmaConfig choose_tma_config(int epi, bool x_bf16, int64_t M, int64_t K, int devi
     c.nch = 2;
     c.G = 32 * ((H + 63) / 64);
   }
-  // rows per group and stage: 4, or 2 when two stages of 4 rows would not
-  // fit beside the pair table (very long rows)
   // rows per group and stage: 8 for one-chunk shapes (long per-warp work
   // amortizes the per-stage reduction; measured best for 2048 x 11008 and
   // 13824 x 5120), else 4; fewer when two stages would not fit beside the
