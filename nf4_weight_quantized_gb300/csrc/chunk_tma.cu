@@ -218,6 +218,14 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 // the CTA-barrier-ordered, memory operations around a ticket atomic).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Load with acquire semantics at GPU scope (a ticket read before the partials
+// it guards).
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -237,6 +245,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const long long u0 = unit_start(blockIdx.x, a);
   const long long u1 = unit_start(blockIdx.x + 1, a);
   const int nq = (int)(u1 - u0);
+  // Processing order.  When the block's last tile continues in the next
+  // block, this block takes that tile's units (its head) first, so their
+  // partial is published early and the next block, which reaches the rest of
+  // that tile at its own end, finds it published and needs not publish its
+  // own.  All roles walk the units in this order: the q-th unit processed is
+  // slice kq_of(q) of tile tile_of(q), and seg_end(q) ends the run of units
+  // of the same tile that holds q (32-bit arithmetic per unit).
+  const int tB = nq > 0 ? (int)((u1 - 1) / a.NQ) : 0;
+  const long long uB = (long long)tB * a.NQ;
+  const int nh = (a.maxseg != 0 && uB > u0 && (u1 % a.NQ) != 0) ? (int)(u1 - uB) : 0;
+  const int t0 = (int)(u0 / a.NQ), r0 = (int)(u0 % a.NQ);
+  auto kq_of = [&](int q) -> int { return q < nh ? q : (r0 + q - nh) % a.NQ; };
+  auto tile_of = [&](int q) -> int { return q < nh ? tB : t0 + (r0 + q - nh) / a.NQ; };
+  auto seg_end = [&](int q) -> int {
+    if (q < nh) return nh;
+    const int e = q + a.NQ - (r0 + q - nh) % a.NQ;
+    return e < nq ? e : nq;
+  };
 
   uint8_t* cst0 = smem + LUT_BYTES;         // SC code stages: codes, then scales
   uint8_t* xst0 = cst0 + SC * CST_BYTES;     // SX X stages
@@ -295,8 +321,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // each completing on its stage's full barrier
   auto issue_codes = [&](int q) {
     const int s = q % SC;
-    const long long u = u0 + q;
-    const int tile = (int)(u / a.NQ), kq = (int)(u % a.NQ);
+    const int tile = tile_of(q), kq = kq_of(q);
     uint8_t* st = cst0 + s * CST_BYTES;
     mbar_arrive_expect_tx(c_full(s), CST_BYTES);
     tma_load_2d(smem_addr(st), &tm_codes, kq * 128, tile * TM, c_full(s));
@@ -304,7 +329,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   };
   auto issue_x = [&](int q) {
     const int s = q % SX;
-    const int kq = (int)((u0 + q) % a.NQ);
+    const int kq = kq_of(q);
     uint8_t* st = xst0 + s * XST_BYTES;
     mbar_arrive_expect_tx(x_full(s), XST_BYTES);
 #pragma unroll
@@ -375,9 +400,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t idesc = idesc_bf16_f32(TM, TN);
       int g = 0;
       for (int q = 0; q < nq;) {
-        const long long tile = (u0 + q) / a.NQ;
         const int qs = q;
-        const int qe = (int)((tile + 1) * a.NQ - u0 < nq ? (tile + 1) * a.NQ - u0 : nq);
+        const int qe = seg_end(q);
         const int buf = g & 1;
         if (g >= 2) mbar_wait_warp(acc_empty(buf), (uint32_t)(((g >> 1) - 1) & 1), abort, lane, 0);
         tc_fence_after_sync();
@@ -484,8 +508,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     pdl_wait();  // Y and the workspace are written only after the previous kernel has finished
     int g = 0;
     for (int q = 0; q < nq; ++g) {
-      const long long tile = (u0 + q) / a.NQ;
-      const int qe = (int)((tile + 1) * a.NQ - u0 < nq ? (tile + 1) * a.NQ - u0 : nq);
+      const long long tile = tile_of(q);
+      const int qe = seg_end(q);
       const bool two = qe - q >= 2;  // the second issuer's chain holds units of this tile
       q = qe;
       const int buf = g & 1;
@@ -521,24 +545,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       // partial tile: the last of the tile's blocks to arrive adds all of them in block order
       const int si = (int)blockIdx.x - bf;
-      float* slot = a.partial + ((long long)tile * a.maxseg + si) * a.N * TM;
-      if (ok && !*abort) {
+      // A tile of two segments whose other partial is already published
+      // (ticket = 1, read with acquire by thread 0; the barrier orders that
+      // read before every thread's loads of the partial): this block is the
+      // last and finishes the tile without publishing its own (s_last = 2).
+      if (tid == 0) s_last = (nseg == 2 && ld_acquire_gpu(a.tickets + tile) == 1u) ? 2u : 0u;
+      named_bar_sync(1, EPI_WARPS * 32);
+      if (s_last == 0u) {
+        float* slot = a.partial + ((long long)tile * a.maxseg + si) * a.N * TM;
+        if (ok && !*abort) {
 #pragma unroll
-        for (int n = 0; n < TN; ++n)
-          if (n < a.N) slot[n * TM + er] = __uint_as_float(acc[n]);
+          for (int n = 0; n < TN; ++n)
+            if (n < a.N) slot[n * TM + er] = __uint_as_float(acc[n]);
+        }
+        // Publish the partial: the barrier orders every epilogue thread's
+        // stores before thread 0, whose release fence (cumulative) then
+        // precedes its ticket; the last arriver's acquire fence follows its
+        // ticket, and the barrier orders it before every thread's loads of
+        // the other partials.
+        named_bar_sync(1, EPI_WARPS * 32);
+        if (tid == 0) {
+          fence_acq_rel_gpu();
+          const unsigned int prev = atomicAdd(&a.tickets[tile], 1u);
+          s_last = (prev == (unsigned int)nseg - 1) ? 1u : 0u;
+          if (s_last) fence_acq_rel_gpu();
+        }
+        named_bar_sync(1, EPI_WARPS * 32);
       }
-      // Publish the partial: the barrier orders every epilogue thread's stores
-      // before thread 0, whose release fence (cumulative) then precedes its
-      // ticket; the last arriver's acquire fence follows its ticket, and the
-      // barrier orders it before every thread's loads of the other partials.
-      named_bar_sync(1, EPI_WARPS * 32);
-      if (tid == 0) {
-        fence_acq_rel_gpu();
-        const unsigned int prev = atomicAdd(&a.tickets[tile], 1u);
-        s_last = (prev == (unsigned int)nseg - 1) ? 1u : 0u;
-        if (s_last) fence_acq_rel_gpu();
-      }
-      named_bar_sync(1, EPI_WARPS * 32);
       if (s_last) {
         // all of a slot's values are loaded before any store (32 independent
         // loads per slot, not one round trip per value); slots added in order
