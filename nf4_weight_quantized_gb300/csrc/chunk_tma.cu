@@ -60,16 +60,16 @@ constexpr int XPROD_WARP = DQ_WARP0 + NDQ;       // 22: the X-ring producer
 constexpr int MMA2_WARP = XPROD_WARP + 1;        // 23: the second MMA issuer
 constexpr int NTHREADS = (MMA2_WARP + 1) * 32;   // 768
 #ifndef NF4_CHUNK_SC
-#define NF4_CHUNK_SC 5
+#define NF4_CHUNK_SC 3
 #endif
 #ifndef NF4_CHUNK_SX
-#define NF4_CHUNK_SX 4
+#define NF4_CHUNK_SX 6
 #endif
 #ifndef NF4_CHUNK_SA
 #define NF4_CHUNK_SA 3
 #endif
 #ifndef NF4_DQ_SLEEP
-#define NF4_DQ_SLEEP 64
+#define NF4_DQ_SLEEP 0
 #endif
 constexpr int SC = NF4_CHUNK_SC;  // code stages (codes + scales of a unit) in shared memory
 constexpr int SX = NF4_CHUNK_SX;  // X stages (the unit's four X slices) in shared memory
