@@ -91,6 +91,55 @@ def test_gemv_shapes(nf4, M, K, xd):
     assert np.all(yh[M:] == 12345.0), "wrote past the output"
 
 
+def _wide_x(seed: int, K: int) -> np.ndarray:
+    """bf16 x whose magnitudes span 2^-60 .. 2^40 inside every 32-element slice."""
+    g = synth.rng(seed, 7)
+    mag = np.exp2(g.integers(-60, 41, size=K)).astype(np.float64)
+    v = (g.choice([-1.0, 1.0], size=K) * mag * g.uniform(1.0, 2.0, size=K)).astype(np.float32)
+    return synth.f32_bits_to_bf16(v)
+
+
+@pytest.mark.parametrize("M,K", [(300, 2048), (64, 11008), (33, 5120)])
+def test_gemv_x_spanning_2_to_the_100(nf4, M, K):
+    # exact fp32 levels: every level * x product is exact inside the FMA, so
+    # x values 2^100 apart within one thread's slice keep the kernel within
+    # its fp32 summation bound of the oracle
+    seed = 170 + M
+    codes, scales = H.quantized(seed, 0, M, K)
+    x = _wide_x(seed, K)
+    y_ref, S = oracle.gemv(codes, scales, x)
+    y = nf4.nf4_gemv(H.weight_tensors(codes, scales), H.x_tensor(x)).cpu().numpy().astype(np.float64)
+    H.assert_within(y, y_ref, S, what=f"wide-range x {M}x{K}")
+    assert np.all(np.abs(y - y_ref) <= KERNEL_REL * S), np.max(np.abs(y - y_ref) / S)
+
+
+def test_opt_in_fp16_levels_within_bound():
+    # the opt-in fp16-level loop (NF4_LUT=1, read when a shape is first
+    # configured, so in a child process): within the 2e-3 * S bound on normal
+    # and on wide-range x (values far below a slice's maximum lose bits, but
+    # their terms are as small inside S)
+    import subprocess
+    import sys
+    import os
+    child = (
+        "import numpy as np, torch, oracle\n"
+        "from nf4_weight_quantized_gb300 import nf4, synth\n"
+        "from tests import helpers as H\n"
+        "from tests.test_gpu_gemv import _wide_x\n"
+        "for M, K, wide in [(300, 2048, False), (2049, 11008, False), (300, 2048, True), (64, 11008, True)]:\n"
+        "    codes, scales = H.quantized(180 + M, 0, M, K)\n"
+        "    x = _wide_x(180 + M, K) if wide else H.make_x(180 + M, K, 'bf16')\n"
+        "    y_ref, S = oracle.gemv(codes, scales, x)\n"
+        "    y = nf4.nf4_gemv(H.weight_tensors(codes, scales), H.x_tensor(x)).cpu().numpy()\n"
+        "    H.assert_within(y, y_ref, S, what=f'fp16 levels {M}x{K} wide={wide}')\n"
+        "    assert 'fp16-level' in nf4.nf4_describe_config(M, K, 1), nf4.nf4_describe_config(M, K, 1)\n"
+        "print('ok')\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, NF4_LUT="1")
+    r = subprocess.run([sys.executable, "-c", child], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+
+
 @pytest.mark.parametrize("M,K", [(300, 2048), (2049, 11008), (77, 5120)])
 def test_register_kernel_path(nf4, M, K):
     # scales that are 4- but not 16-byte aligned take the register-prefetch
