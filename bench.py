@@ -168,7 +168,7 @@ def describe(nf4, w) -> str:
     if w.kind == "rmsnorm":
         return f"nf4_rmsnorm: {w.M} row(s) of {w.K}, one block per row, bf16 out"
     rows = 2 * w.M if w.kind == "glu" else w.M + 2 * w.M_kv
-    return nf4.nf4_describe_config(rows, w.K, w.N)
+    return nf4.nf4_describe_launch(w.kind, rows, w.K, w.N)
 
 
 def build_calls(name: str, torch, nf4, synth, device, copies=None):
@@ -558,7 +558,7 @@ def run_gpu(args, rank, world, dist):
         "config": {"workload": WORKLOAD_NAME,
                    "l2": f"rotating {copies} weight copies ({copies * b['weight'] / 1e6:.0f} MB, >3x L2)",
                    "parallelism": "replicas" if world > 1 else "single",
-                   "kernel": nf4.nf4_describe_config(2048, 11008, 1)},
+                   "kernel": nf4.nf4_describe_launch("residual", 2048, 11008, 1)},
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": args.steps,

@@ -308,6 +308,14 @@ const char* nf4_last_error(void);
  * The string is thread-local and valid until the next call on this thread. */
 const char* nf4_describe_config(int64_t M, int64_t K, int N);
 
+/* The same for one operation, whose epilogue can change the launch (its
+ * register use sets how many row groups fit in a block): op is "gemv",
+ * "residual", "swiglu", "glu", "qkv", "argmax" (N = 1, bf16 x; M counts all
+ * rows of the launch: 2 x outputs for "glu", q + k + v rows for "qkv") or
+ * "chunk" (N in [1, 32]).  nf4_describe_config(M, K, N) is "gemv" at N = 1
+ * and "chunk" otherwise.  An unknown op gives a message saying so. */
+const char* nf4_describe_launch(const char* op, int64_t M, int64_t K, int N);
+
 #ifdef __cplusplus
 }
 #endif

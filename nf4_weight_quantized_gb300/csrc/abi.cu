@@ -492,7 +492,24 @@ void nf4_codebook(float out[16]) {
 const char* nf4_last_error(void) { return g_last_error.c_str(); }
 
 const char* nf4_describe_config(int64_t M, int64_t K, int N) {
-  if (check_shape(M, K, "nf4_describe_config") || N < 1 || N > NF4_MAX_CHUNK_N) {
+  return nf4_describe_launch(N == 1 ? "gemv" : "chunk", M, K, N);
+}
+
+const char* nf4_describe_launch(const char* op, int64_t M, int64_t K, int N) {
+  static const struct {
+    const char* name;
+    int epi;
+  } kOps[] = {{"gemv", nf4k::EPI_PLAIN},   {"residual", nf4k::EPI_RESID}, {"swiglu", nf4k::EPI_SWIGLU},
+              {"glu", nf4k::EPI_GLU},      {"qkv", nf4k::EPI_QKV},        {"argmax", nf4k::EPI_ARGMAX},
+              {"chunk", -1}};
+  int epi = -2;
+  for (const auto& o : kOps)
+    if (op && std::strcmp(op, o.name) == 0) epi = o.epi;
+  if (epi == -2 || (epi == -1) != (N > 1 || (op && std::strcmp(op, "chunk") == 0))) {
+    g_describe = std::string("invalid operation: ") + (op ? op : "(null)") + " at N = " + std::to_string(N);
+    return g_describe.c_str();
+  }
+  if (check_shape(M, K, "nf4_describe_launch") || N < 1 || N > NF4_MAX_CHUNK_N) {
     g_describe = std::string("invalid shape: ") + g_last_error;
     return g_describe.c_str();
   }
@@ -503,15 +520,15 @@ const char* nf4_describe_config(int64_t M, int64_t K, int N) {
   }
   char buf[512];
   const nf4k::ClusterConfig cc =
-      (N == 1 && !use_register_kernel()) ? nf4k::choose_cluster_config(nf4k::EPI_PLAIN, M, K, dev) : nf4k::ClusterConfig{};
+      (epi >= 0 && !use_register_kernel()) ? nf4k::choose_cluster_config(epi, M, K, dev) : nf4k::ClusterConfig{};
   if (cc.ok) {
     std::snprintf(buf, sizeof buf,
                   "gemv M=%lld K=%lld: cluster split-K kernel, %d clusters of %d blocks (K split %d ways, %d rows per "
                   "cluster), %d threads per block, partial sums added through distributed shared memory, %s",
                   (long long)M, (long long)K, cc.clusters, cc.CL, cc.CL, cc.RPC, cc.threads,
                   nf4k::pdl_enabled() ? "programmatic dependent launch" : "plain launch");
-  } else if (N == 1) {
-    const nf4k::TmaConfig t = use_register_kernel() ? nf4k::TmaConfig{} : nf4k::choose_tma_config(nf4k::EPI_PLAIN, true, M, K, dev);
+  } else if (epi >= 0) {
+    const nf4k::TmaConfig t = use_register_kernel() ? nf4k::TmaConfig{} : nf4k::choose_tma_config(epi, true, M, K, dev);
     if (t.ok) {
       std::snprintf(buf, sizeof buf,
                     "gemv M=%lld K=%lld (16-byte aligned scales): bulk-copy kernel, %d thread(s) per row, %d row(s) "
@@ -521,7 +538,7 @@ const char* nf4_describe_config(int64_t M, int64_t K, int N) {
                     t.smem, t.lut == 1 ? "fp16-level mixed-precision loop for bf16 x" : "fp32 pair",
                     nf4k::pdl_enabled() ? "programmatic dependent launch" : "plain launch");
     } else {
-      const nf4k::GemvConfig c = nf4k::choose_gemv_config(nf4k::EPI_PLAIN, M, K, dev);
+      const nf4k::GemvConfig c = nf4k::choose_gemv_config(epi, M, K, dev);
       std::snprintf(buf, sizeof buf,
                     "gemv M=%lld K=%lld: register kernel, %d thread(s) per row (%d chunk(s) of 32 weights each), %d "
                     "row(s) per batch, %d row group(s) per block, %d blocks of %d threads, %d B shared memory%s",

@@ -73,6 +73,8 @@ def _load():
     lib.nf4_last_error.restype = ctypes.c_char_p
     lib.nf4_describe_config.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
     lib.nf4_describe_config.restype = ctypes.c_char_p
+    lib.nf4_describe_launch.argtypes = [ctypes.c_char_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
+    lib.nf4_describe_launch.restype = ctypes.c_char_p
     lib.nf4_check_device_errors.argtypes = []
     lib.nf4_check_device_errors.restype = ctypes.c_int
     lib.nf4_debug_set_wait_limit.argtypes = [ctypes.c_uint32]
@@ -84,7 +86,7 @@ lib = _load()
 
 EXPORTS = ("nf4_gemv", "nf4_gemv_residual", "nf4_gemv_swiglu", "nf4_gemv_argmax", "nf4_gemm_chunk",
            "nf4_workspace_bytes", "nf4_quantize", "nf4_codebook", "nf4_last_error", "nf4_describe_config",
-           "nf4_check_device_errors", "nf4_gemm_chunk_noalloc", "nf4_gemv_qkv",
+           "nf4_describe_launch", "nf4_check_device_errors", "nf4_gemm_chunk_noalloc", "nf4_gemv_qkv",
            "nf4_dequant_rows", "nf4_gemv_glu_interleaved", "nf4_debug_set_wait_limit", "nf4_rmsnorm")
 
 
@@ -304,6 +306,10 @@ def nf4_codebook() -> list[float]:
 
 def nf4_describe_config(M: int, K: int, N: int = 1) -> str:
     return lib.nf4_describe_config(M, K, N).decode()
+
+
+def nf4_describe_launch(op: str, M: int, K: int, N: int = 1) -> str:
+    return lib.nf4_describe_launch(op.encode(), M, K, N).decode()
 
 
 def nf4_check_device_errors() -> None:

@@ -108,6 +108,9 @@ def test_no_device_is_reported_not_faked(nf4):
 
 def test_describe_config_rejects_bad_shape(nf4):
     assert "invalid shape" in nf4.nf4_describe_config(8, 100, 1)
+    assert "invalid operation" in nf4.nf4_describe_launch("transpose", 8, 128, 1)
+    assert "invalid operation" in nf4.nf4_describe_launch("residual", 8, 128, 4)  # N > 1 is the chunk only
+    assert "invalid shape" in nf4.nf4_describe_launch("residual", 8, 100, 1)
 
 
 def test_noalloc_rejects_oversize_before_any_device_work(nf4):
