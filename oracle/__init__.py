@@ -55,8 +55,29 @@ def load():
     for name in ("nf4o_codebook", "nf4o_quantize", "nf4o_dequant", "nf4o_gemv", "nf4o_gemv_residual",
                  "nf4o_gemv_swiglu", "nf4o_gemv_argmax", "nf4o_gemm_chunk"):
         getattr(lib, name).restype = ctypes.c_int
+    # the library's calls on the host (nf4_ref_*), weight descriptors by pointer
+    W = ctypes.POINTER(RefWeight)
+    ref = {"nf4_ref_quantize": [P, I64, I64, P, P], "nf4_ref_gemv": [W, P, I, P],
+           "nf4_ref_gemv_residual": [W, P, I, P, P], "nf4_ref_gemv_swiglu": [W, W, P, I, P],
+           "nf4_ref_gemv_glu_interleaved": [W, P, I, P], "nf4_ref_gemv_qkv": [W, W, W, P, P, P, P, I, P, P, P],
+           "nf4_ref_gemv_argmax": [W, P, I, P, P], "nf4_ref_gemm_chunk": [W, P, I, P],
+           "nf4_ref_dequant_rows": [W, P, I64, P, I], "nf4_ref_rmsnorm": [P, P, I64, I64, ctypes.c_float, P, I]}
+    for name, args in ref.items():
+        getattr(lib, name).argtypes = args
+        getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
+
+
+class RefWeight(ctypes.Structure):
+    """Weight descriptor of the nf4_ref_* calls (host pointers): codes, scales, M, K."""
+
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("M", ctypes.c_int64),
+                ("K", ctypes.c_int64)]
+
+    @classmethod
+    def of(cls, codes: np.ndarray, scales: np.ndarray) -> "RefWeight":
+        return cls(codes.ctypes.data, scales.ctypes.data, codes.shape[0], codes.shape[1] * 2)
 
 
 def _ptr(a):

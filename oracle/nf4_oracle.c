@@ -38,6 +38,10 @@
  *    before the product, as the chunk's tensor-core path does; the sum is float64.
  *
  * No blocking, fusion or reordering beyond these definitions.
+ *
+ * The nf4o_* functions take per-row selections and return float64 values (and
+ * the magnitudes S) for the tests; the nf4_ref_* functions at the end take the
+ * library's own argument lists with host pointers and return its output types.
  */
 #include <math.h>
 #include <stddef.h>
@@ -460,3 +464,119 @@ int nf4o_rmsnorm(const float* x, const uint16_t* w, int64_t rows, int64_t K, dou
 
 /* Rounding helpers exposed for the tests: double -> bf16 bits (RN-even). */
 uint16_t nf4o_round_bf16(double v) { return f64_to_bf16_bits(v); }
+
+/* ------------------------------------------------ the library's calls, on the host
+ *
+ * nf4_ref_* take the arguments of the library's calls of the same name
+ * (nf4_gemv, ..., nf4_gemm_chunk, without the stream and the workspace) with
+ * host pointers, and compute them as defined above: float64 sums, epilogues in
+ * float64, each result rounded once to the output type (fp32 by C's
+ * double -> float conversion, round to nearest even; bf16 by
+ * f64_to_bf16_bits).  The weight descriptor is this file's own, with the same
+ * members in the same order as the library's.  Each returns 0, or -1 for an
+ * invalid argument (nothing is written then for the shape checks; the others
+ * may stop part way).  Activation and output dtypes: 0 = fp32, 1 = bf16.
+ */
+typedef struct nf4_ref_weight {
+  const uint8_t* codes; /* [M][K/2] */
+  const float* scales;  /* [M][K/64] */
+  int64_t M;
+  int64_t K;
+} nf4_ref_weight;
+
+static int ref_ok(const nf4_ref_weight* W) { return W && W->codes && W->scales && shape_ok(W->M, W->K); }
+
+int nf4_ref_quantize(const float* W, int64_t M, int64_t K, uint8_t* codes, float* scales) {
+  return nf4o_quantize(W, M, K, codes, scales);
+}
+
+int nf4_ref_gemv(const nf4_ref_weight* W, const void* x, int xt, float* y) {
+  if (!ref_ok(W) || !y) return NF4O_EINVAL;
+  for (int64_t m = 0; m < W->M; ++m) {
+    double v;
+    int st = nf4o_gemv(W->codes, W->scales, W->M, W->K, x, xt, &m, 1, &v, NULL);
+    if (st) return st;
+    y[m] = (float)v;
+  }
+  return NF4O_OK;
+}
+
+/* y may alias residual: row m's residual is read before y[m] is written. */
+int nf4_ref_gemv_residual(const nf4_ref_weight* W, const void* x, int xt, const float* residual, float* y) {
+  if (!ref_ok(W) || !residual || !y) return NF4O_EINVAL;
+  return nf4o_gemv_residual(W->codes, W->scales, W->M, W->K, x, xt, residual, NULL, 0, NULL, y);
+}
+
+int nf4_ref_gemv_swiglu(const nf4_ref_weight* Wg, const nf4_ref_weight* Wu, const void* x, int xt, uint16_t* out) {
+  if (!ref_ok(Wg) || !ref_ok(Wu) || Wg->M != Wu->M || Wg->K != Wu->K || !out) return NF4O_EINVAL;
+  return nf4o_gemv_swiglu(Wg->codes, Wg->scales, Wu->codes, Wu->scales, Wg->M, Wg->K, x, xt, NULL, 0, NULL, out,
+                          NULL, NULL);
+}
+
+int nf4_ref_gemv_glu_interleaved(const nf4_ref_weight* W, const void* x, int xt, uint16_t* out) {
+  if (!ref_ok(W) || !out) return NF4O_EINVAL;
+  return nf4o_gemv_glu_interleaved(W->codes, W->scales, W->M, W->K, x, xt, NULL, 0, NULL, out, NULL, NULL);
+}
+
+/* q/k/v: each output gets its matrix's float64 sum plus its bias (bias may be NULL). */
+int nf4_ref_gemv_qkv(const nf4_ref_weight* Wq, const nf4_ref_weight* Wk, const nf4_ref_weight* Wv, const float* bq,
+                     const float* bk, const float* bv, const void* x, int xt, float* q, float* k, float* v) {
+  const nf4_ref_weight* W[3] = {Wq, Wk, Wv};
+  const float* b[3] = {bq, bk, bv};
+  float* out[3] = {q, k, v};
+  for (int p = 0; p < 3; ++p)
+    if (!ref_ok(W[p]) || W[p]->K != Wq->K || !out[p]) return NF4O_EINVAL;
+  for (int p = 0; p < 3; ++p)
+    for (int64_t m = 0; m < W[p]->M; ++m) {
+      double s;
+      int st = nf4o_gemv(W[p]->codes, W[p]->scales, W[p]->M, W[p]->K, x, xt, &m, 1, &s, NULL);
+      if (st) return st;
+      out[p][m] = (float)(s + (b[p] ? (double)b[p][m] : 0.0));
+    }
+  return NF4O_OK;
+}
+
+int nf4_ref_gemv_argmax(const nf4_ref_weight* W, const void* x, int xt, float* logits, int64_t* index) {
+  if (!ref_ok(W) || !logits || !index) return NF4O_EINVAL;
+  return nf4o_gemv_argmax(W->codes, W->scales, W->M, W->K, x, xt, NULL, logits, index);
+}
+
+/* Y[n][m], X bf16 bits [N][K]; N in [1, 32] as the library's call. */
+int nf4_ref_gemm_chunk(const nf4_ref_weight* W, const uint16_t* X, int N, float* Y) {
+  if (!ref_ok(W) || !X || !Y || N < 1 || N > 32) return NF4O_EINVAL;
+  for (int64_t m = 0; m < W->M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double s;
+      int st = nf4o_gemm_chunk(W->codes, W->scales, W->M, W->K, X + n * W->K, 1, &m, 1, &s, NULL);
+      if (st) return st;
+      Y[n * W->M + m] = (float)s;
+    }
+  return NF4O_OK;
+}
+
+/* Rows E[ids[i]] as fp32 (ot 0) or bf16 (ot 1); an id outside [0, M) gives a
+ * row of zeros, as the library writes it (which also reports it). */
+int nf4_ref_dequant_rows(const nf4_ref_weight* E, const int64_t* ids, int64_t n, void* out, int ot) {
+  if (!ref_ok(E) || (n > 0 && (!ids || !out)) || n < 0 || (ot != NF4O_F32 && ot != NF4O_BF16)) return NF4O_EINVAL;
+  int64_t bad = 0;
+  return nf4o_dequant_rows(E->codes, E->scales, E->M, E->K, ids, n, ot == NF4O_F32 ? (float*)out : NULL,
+                           ot == NF4O_BF16 ? (uint16_t*)out : NULL, &bad);
+}
+
+/* y fp32 (yt 0, may equal x) or bf16 (yt 1); eps widened exactly to float64. */
+int nf4_ref_rmsnorm(const float* x, const uint16_t* w, int64_t rows, int64_t K, float eps, void* y, int yt) {
+  if (!x || !w || !y || rows < 1 || K < 1 || !(eps >= 0.0f) || (yt != NF4O_F32 && yt != NF4O_BF16)) return NF4O_EINVAL;
+  for (int64_t r = 0; r < rows; ++r) {
+    double ss = 0.0;
+    for (int64_t k = 0; k < K; ++k) ss += (double)x[r * K + k] * (double)x[r * K + k];
+    const double inv = 1.0 / sqrt(ss / (double)K + (double)eps);
+    for (int64_t k = 0; k < K; ++k) {
+      const double v = (double)x[r * K + k] * inv * (double)bf16_bits_to_f32(w[k]);
+      if (yt == NF4O_F32)
+        ((float*)y)[r * K + k] = (float)v;
+      else
+        ((uint16_t*)y)[r * K + k] = f64_to_bf16_bits(v);
+    }
+  }
+  return NF4O_OK;
+}

@@ -702,3 +702,73 @@ def test_rmsnorm_rejects_bad_arguments(oracle_mod):
         oracle_mod.rmsnorm(np.ones(4, np.float32), np.ones(3, np.uint16), 0.0)
     with pytest.raises(ValueError):
         oracle_mod.rmsnorm(np.ones(4, np.float32), np.ones(4, np.uint16), -1.0)
+
+
+def test_ref_entry_points_round_the_float64_results_once(oracle_mod):
+    # nf4_ref_* take the library's arguments with host pointers; each result is
+    # the float64 definition rounded once to the output type
+    import ctypes
+
+    oracle = oracle_mod
+    lib = oracle.load()
+    W_ = oracle.RefWeight
+    M, K = 40, 256
+    W = synth.weights(990, 0, M, K)
+    codes, scales = oracle.quantize(W)
+    c2 = np.zeros_like(codes)
+    s2 = np.zeros_like(scales)
+    assert lib.nf4_ref_quantize(W.ctypes.data, M, K, c2.ctypes.data, s2.ctypes.data) == 0
+    assert np.array_equal(c2, codes) and np.array_equal(s2.view(np.uint32), scales.view(np.uint32))
+    w = W_.of(codes, scales)
+    P = ctypes.byref
+    for xt, x in ((0, synth.normal_f32(990, 1, K)), (1, synth.normal_bf16(990, 1, K))):
+        y64, _ = oracle.gemv(codes, scales, x)
+        y = np.zeros(M, np.float32)
+        assert lib.nf4_ref_gemv(P(w), x.ctypes.data, xt, y.ctypes.data) == 0
+        assert np.array_equal(y, y64.astype(np.float32))
+        r = synth.normal_f32(990, 2, M)
+        ry = r.copy()
+        assert lib.nf4_ref_gemv_residual(P(w), x.ctypes.data, xt, ry.ctypes.data, ry.ctypes.data) == 0  # in place
+        assert np.array_equal(ry, oracle.gemv_residual(codes, scales, x, r)[1])
+        l64, l32, idx = oracle.gemv_argmax(codes, scales, x)
+        lg = np.zeros(M, np.float32)
+        ix = np.zeros(1, np.int64)
+        assert lib.nf4_ref_gemv_argmax(P(w), x.ctypes.data, xt, lg.ctypes.data, ix.ctypes.data) == 0
+        assert np.array_equal(lg, l32) and int(ix[0]) == idx
+    x = synth.normal_bf16(991, 1, K)
+    gc, gs = oracle.quantize(synth.weights(991, 1, M, K))
+    out = np.zeros(M, np.uint16)
+    assert lib.nf4_ref_gemv_swiglu(P(w), P(W_.of(gc, gs)), x.ctypes.data, 1, out.ctypes.data) == 0
+    assert np.array_equal(out, oracle.gemv_swiglu(codes, scales, gc, gs, x)[1])
+    out2 = np.zeros(M // 2, np.uint16)
+    assert lib.nf4_ref_gemv_glu_interleaved(P(w), x.ctypes.data, 1, out2.ctypes.data) == 0
+    assert np.array_equal(out2, oracle.gemv_glu_interleaved(codes, scales, x)[1])
+    bq = synth.normal_f32(992, 3, M)
+    q, k, v = (np.zeros(M, np.float32) for _ in range(3))
+    assert lib.nf4_ref_gemv_qkv(P(w), P(W_.of(gc, gs)), P(w), bq.ctypes.data, None, None, x.ctypes.data, 1,
+                                q.ctypes.data, k.ctypes.data, v.ctypes.data) == 0
+    yq, _ = oracle.gemv_qkv([(codes, scales, bq), (gc, gs, None), (codes, scales, None)], x)
+    assert np.array_equal(np.concatenate([q, k, v]), yq.astype(np.float32))
+    X = synth.normal_bf16(993, 1, 7 * K).reshape(7, K)
+    Y = np.zeros((7, M), np.float32)
+    assert lib.nf4_ref_gemm_chunk(P(w), X.ctypes.data, 7, Y.ctypes.data) == 0
+    assert np.array_equal(Y, oracle.gemm_chunk(codes, scales, X)[0].astype(np.float32))
+    ids = np.array([3, 0, 39, 39, 17], np.int64)
+    rows32 = np.zeros((5, K), np.float32)
+    rows16 = np.zeros((5, K), np.uint16)
+    assert lib.nf4_ref_dequant_rows(P(w), ids.ctypes.data, 5, rows32.ctypes.data, 0) == 0
+    assert lib.nf4_ref_dequant_rows(P(w), ids.ctypes.data, 5, rows16.ctypes.data, 1) == 0
+    f32, b16, bad = oracle.dequant_rows(codes, scales, ids)
+    assert bad == 0 and np.array_equal(rows32, f32) and np.array_equal(rows16, b16)
+    xr = synth.normal_f32(994, 4, 3 * K).reshape(3, K)
+    g = synth.f32_bits_to_bf16((1.0 + 0.25 * synth.normal_f32(994, 5, K)).astype(np.float32))
+    yr = np.zeros((3, K), np.float32)
+    yb = np.zeros((3, K), np.uint16)
+    assert lib.nf4_ref_rmsnorm(xr.ctypes.data, g.ctypes.data, 3, K, ctypes.c_float(1e-6), yr.ctypes.data, 0) == 0
+    assert lib.nf4_ref_rmsnorm(xr.ctypes.data, g.ctypes.data, 3, K, ctypes.c_float(1e-6), yb.ctypes.data, 1) == 0
+    y64, _ = oracle.rmsnorm(xr, g, float(np.float32(1e-6)))
+    assert np.array_equal(yr, y64.astype(np.float32))
+    assert np.array_equal(yb, np.array([[oracle.round_bf16(v) for v in row] for row in y64], np.uint16))
+    # invalid arguments are refused
+    assert lib.nf4_ref_gemv(None, x.ctypes.data, 1, y.ctypes.data) == -1
+    assert lib.nf4_ref_gemm_chunk(P(w), X.ctypes.data, 33, Y.ctypes.data) == -1
