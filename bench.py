@@ -315,6 +315,30 @@ def time_calls(torch, call, copies: int, steps: int, warmup: int, stream, dist=N
     return e0.elapsed_time(e1) / 1e3, clocks
 
 
+def time_windows(torch, call, copies: int, stream, windows: int = 5, calls: int = 500):
+    """Per-call microseconds of `windows` separately timed replays of one graph
+    of `calls` calls (after the main timing, outside `value`): the spread
+    between windows."""
+    n = max(copies, (calls // copies) * copies)
+    g = capture(torch, call, n, 0, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    out = []
+    for _ in range(windows):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        out.append(e0.elapsed_time(e1) * 1e3 / n)
+    srt = sorted(out)
+    return {"calls_per_window": n, "us_per_call": [round(v, 4) for v in out], "median": round(srt[len(srt) // 2], 4),
+            "min": round(srt[0], 4), "max": round(srt[-1], 4)}
+
+
 # ------------------------------------------------------------- CPU baseline
 
 def _oracle_rows_worker(task):
@@ -455,6 +479,7 @@ def run_gpu(args, rank, world, dist):
     secs, clocks = time_calls(torch, call, copies, args.steps, args.warmup, stream, dist,
                               clock_window_s=args.clock_window, sampler=sampler)
     secs = reduce_max(dist, secs, device)
+    windows = time_windows(torch, call, copies, stream)
     per_call = secs / args.steps
     value = replica_value(world, b["weight"], args.steps, secs)
     achieved = b["total"] / per_call / 1e9
@@ -562,6 +587,7 @@ def run_gpu(args, rank, world, dist):
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": args.steps,
+        "windows": windows,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic("down_residual"),
                      "peak_source": peaks["source"], "algorithmic_bytes_per_launch": b["total"]},
