@@ -522,6 +522,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool two = qe - q >= 2;  // the second issuer's chain holds units of this tile
       q = qe;
       const int buf = g & 1;
+      // the tile's segment count and this block's place among them (the
+      // block_of searches) are worked out while the accumulators fill, not
+      // after: on a block's last tile they would delay its end
+      const long long m = tile * TM + er;
+      const int bf = a.maxseg == 0 ? (int)blockIdx.x : block_of(tile * a.NQ, a);
+      const int nseg = a.maxseg == 0 ? 1 : block_of(tile * a.NQ + a.NQ - 1, a) - bf + 1;
+      const int si = (int)blockIdx.x - bf;
       const bool ok = mbar_wait_warp(acc_full(buf), (uint32_t)((g >> 1) & 1), abort, lane, 128);
       tc_fence_after_sync();
       uint32_t acc[32];
@@ -541,9 +548,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(buf));
-      const long long m = tile * TM + er;
-      const int bf = a.maxseg == 0 ? (int)blockIdx.x : block_of(tile * a.NQ, a);
-      const int nseg = a.maxseg == 0 ? 1 : block_of(tile * a.NQ + a.NQ - 1, a) - bf + 1;
       if (nseg == 1) {
         if (ok && !*abort && m < a.M) {
 #pragma unroll
@@ -553,7 +557,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         continue;
       }
       // partial tile: the last of the tile's blocks to arrive adds all of them in block order
-      const int si = (int)blockIdx.x - bf;
       // A tile of two segments whose other partial is already published
       // (ticket = 1, read with acquire by thread 0; the barrier orders that
       // read before every thread's loads of the partial): this block is the
