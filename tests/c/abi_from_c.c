@@ -68,6 +68,8 @@ static void host_checks(void) {
   CHECK(nf4_gemv(&w, (const void*)(uintptr_t)4096, NF4_BF16, (float*)(uintptr_t)4096, NULL) == NF4_EALIGN,
         "unaligned codes accepted");
   CHECK(nf4_workspace_bytes(151936, 2048, 1) >= 16, "argmax workspace");
+  CHECK(strstr(nf4_describe_launch("transpose", 8, 128, 1), "invalid operation") != NULL, "unknown op described");
+  CHECK(strstr(nf4_describe_launch("residual", 8, 100, 1), "invalid shape") != NULL, "K = 100 described");
   printf("host checks ok\n");
 }
 
