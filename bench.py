@@ -63,13 +63,40 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its // and /* */ comments (string and
+    character literals kept as they are), so that a comment edit does not
+    count as a change of the kernels."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            while i < n and src[i] != "\n":
+                i += 1
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash() -> str:
+    """First 16 hex digits of sha256 over the kernel sources (file names and
+    their code, comments removed)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nf4_weight_quantized_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
