@@ -65,8 +65,8 @@ def measured_peaks() -> dict:
 
 def strip_comments(src: str) -> str:
     """C/C++/CUDA source without its // and /* */ comments (string and
-    character literals kept as they are), so that a comment edit does not
-    count as a change of the kernels."""
+    character literals kept as they are), trailing blanks and blank lines, so
+    that editing a comment does not count as a change of the kernels."""
     out, i, n = [], 0, len(src)
     while i < n:
         c = src[i]
@@ -85,7 +85,9 @@ def strip_comments(src: str) -> str:
         else:
             out.append(c)
             i += 1
-    return "".join(out)
+    # lines left empty by a removed comment, and trailing blanks, do not count
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
 
 
 def kernel_source_hash() -> str:

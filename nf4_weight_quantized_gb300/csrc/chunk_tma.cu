@@ -9,7 +9,8 @@
 //
 //  * work units are (128-row tile, 256-column slice) pairs, tile-major; each of
 //    min(units, 152) persistent blocks takes one contiguous, equal share of them
-//    (stream-K), so every SM streams the same number of bytes;
+//    (stream-K), so every SM streams the same number of bytes; a block whose
+//    last tile continues in the next block processes that tile's units first;
 //  * two producer warps load each unit with 2-D TMA copies into two rings: one
 //    the codes (128 rows x 128 bytes, 128-byte swizzled so the dequantizing
 //    threads read them without bank conflicts) and the 128 x 4 fp32 scales into
@@ -24,14 +25,16 @@
 //    rounded once) and store it straight into tensor memory (tcgen05.st; row m
 //    in TMEM lane m), a ring of three stages of four k-tiles: the A operand never passes
 //    through shared memory, which the pair-table reads alone keep busy;
-//  * one thread issues tcgen05.mma (M = 128, N = 32, K = 16, A from TMEM, X from
-//    shared memory) into one of two TMEM accumulator buffers, so four epilogue
-//    warps can drain one tile while the next accumulates; each buffer holds
-//    two 32-column chains that consecutive MMAs alternate between (an MMA
-//    never waits for the previous one's accumulation), added in the epilogue;
+//  * two issuer warps (one thread each) issue tcgen05.mma (M = 128, N = 32,
+//    K = 16, A from TMEM, X from shared memory) into one of two TMEM
+//    accumulator buffers, so four epilogue warps can drain one tile while the
+//    next accumulates; within a tile the units alternate between the issuers,
+//    each accumulating into its own 32-column chain of the buffer, and the
+//    epilogue adds the two chains;
 //  * a tile whose K range is split over several blocks is finished by the last of
 //    them to arrive (a per-tile ticket), which adds the partial tiles in block
-//    order: the result does not depend on timing.
+//    order: the result does not depend on timing.  The last of two that finds
+//    the other's partial already published does not publish its own.
 // Every wait is bounded; on a timeout the block stops issuing work, waits for its
 // copies and tensor-core operations, frees its TMEM and reports the error word.
 #include <cuda.h>

@@ -22,7 +22,7 @@
 //
 // Dequantization modes (LUTM):
 //  LUT_F32     pair table of exact fp32 levels: per code byte one PRMT, one
-//              conflict-free LDS.64 and one packed fma.rn.f32x2.  Bound by
+//              conflict-free LDS.64 and two FFMAs.  Bound by
 //              shared-memory bandwidth (8 bytes per two weights).  The default
 //              for every activation dtype.
 //  LUT_F16MIX  opt-in for bf16 activations (NF4_LUT=1): pair table of
