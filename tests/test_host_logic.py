@@ -157,3 +157,49 @@ def test_reference_arm_line():
 def test_reference_arm_other_ranks_print_nothing():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
     assert _bench_lines("--impl", "reference", "--steps", "2", "--warmup", "3", env=env) == []
+
+
+def _chunk_plan(M, K, B=152):
+    """The stream-K plan of the TMA chunk kernel, restated: (tiles, units per
+    tile, units, blocks, partial slots per tile, first unit of each block)."""
+    tiles, NQ = (M + 127) // 128, K // 256
+    U = tiles * NQ
+    Bn = max(1, min(U, B))
+    if tiles >= 4 * Bn:
+        return tiles, NQ, U, Bn, 0, [(b * tiles // Bn) * NQ for b in range(Bn + 1)]
+    mu = U // Bn
+    return tiles, NQ, U, Bn, min((NQ + mu - 1) // mu + 1, Bn), [b * U // Bn for b in range(Bn + 1)]
+
+
+@pytest.mark.parametrize("M,K,N", [(13824, 5120, 32), (2048, 2048, 7), (5120, 27648, 16), (1000, 512, 3),
+                                   (300, 65536, 32), (27648, 5120, 32), (128, 256, 1)])
+def test_chunk_processing_order_and_partial_slots(nf4_lib, M, K, N):
+    # every unit is processed by exactly one block; a block's runs of units stay
+    # inside one tile; a block takes the head of its last tile first only when
+    # that tile continues in the next block; no tile spans more blocks than it
+    # has partial slots, and the library's workspace holds them all
+    tiles, NQ, U, B, maxseg, start = _chunk_plan(M, K)
+    seen = []
+    for b in range(B):
+        u0, u1 = start[b], start[b + 1]
+        nq = u1 - u0
+        tB = (u1 - 1) // NQ
+        uB = tB * NQ
+        nh = u1 - uB if (maxseg and uB > u0 and u1 % NQ) else 0
+        r0 = u0 % NQ
+        unit = [uB + q if q < nh else u0 + q - nh for q in range(nq)]
+        seen += unit
+        q = 0
+        while q < nq:  # seg_end as the kernel computes it
+            e = nh if q < nh else min(q + NQ - (r0 + q - nh) % NQ, nq)
+            assert e > q and len({unit[i] // NQ for i in range(q, e)}) == 1
+            assert all(unit[i + 1] == unit[i] + 1 for i in range(q, e - 1))
+            q = e
+    assert sorted(seen) == list(range(U))
+    if maxseg:
+        owners = {}
+        for b in range(B):
+            for u in range(start[b], start[b + 1]):
+                owners.setdefault(u // NQ, set()).add(b)
+        assert max(len(v) for v in owners.values()) <= maxseg
+        assert nf4_lib.nf4_workspace_bytes(M, K, N) >= tiles * maxseg * N * 128 * 4 + tiles * 4 + 16
