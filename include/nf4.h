@@ -31,16 +31,20 @@
  *   - Inputs are never written, except that nf4_gemv_residual's `y` may alias
  *     `residual`.  Any other overlap between an output and an input is
  *     undefined behaviour.
- *   - N=1 kernels use programmatic dependent launch: they may start, and read
- *     (or prefetch) the weights, before the previous kernel on the stream has
- *     finished when that kernel allows it; activations and outputs are touched
- *     only after it finishes.  So weights must not be written by the kernel
- *     launched just before on the same stream if that kernel triggers its
- *     dependents early (no kernel of this library that writes weights does).
+ *   - The N=1 kernels, the prefill-chunk kernel and nf4_rmsnorm use
+ *     programmatic dependent launch: they may start, and read (or prefetch)
+ *     the weights (nf4_rmsnorm: its gain), before the previous kernel on the
+ *     stream has finished when that kernel allows it; activations, outputs and
+ *     workspaces are touched only after it finishes.  So weights and gains must
+ *     not be written by the kernel launched just before on the same stream if
+ *     that kernel triggers its dependents early (no kernel of this library
+ *     that writes weights does).  NF4_PDL=0 in the environment turns this off.
  *   - Arguments are validated on the host before any launch; a failed call
  *     launches nothing and returns a negative nf4_status.  nf4_last_error()
- *     gives a message for the calling thread's last failure.  Kernels do not
- *     report errors; invalid device pointers are undefined behaviour.
+ *     gives a message for the calling thread's last failure.  Kernels report
+ *     only a bounded wait that ran out and token ids outside their table,
+ *     through nf4_check_device_errors; invalid device pointers are undefined
+ *     behaviour.
  *   - Alignment: codes and x / X must be 16-byte aligned; scales, y, residual,
  *     logits and Y 4-byte aligned; out 2-byte; index and workspace 8-byte.
  *   - Sizes: K a positive multiple of 64 and at most NF4_MAX_K; 1 <= M < 2^31.
